@@ -1,0 +1,272 @@
+/*
+ * tp.h — C ABI of the tensor-parallel (TP) Llama decoder forward, with the t
+ * ranks of a TP group emulated as shard buffers on one GPU.
+ *
+ * What the calls compute follows three pages on Megatron-style tensor
+ * parallelism in LLM inference engines:
+ *   [P1] "第 9 章 多进程与张量并行" (zero-to-sglang), §3.1 通信, §3.2 切分
+ *   [P2] "Tensor Parallelism 执行路径" (sglang-internals), 前向执行的实际流程,
+ *        KV Cache 在 TP 下怎样分布
+ *   [P3] "张量、流水线与数据并行" (inference/05-parallel/tensor-parallel),
+ *        线性层怎么切, 每 token 的通信量（估算）
+ *
+ * Conventions for every call
+ *   - Pointers named in the signatures are DEVICE pointers unless stated
+ *     otherwise.  bf16 values travel as raw 16-bit patterns (tp_bf16).
+ *   - Matrices are row-major.  Weights use the [out, in] layout.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on it, except tp_load_shards and tp_check_device, which
+ *     synchronise it.  Nothing on the forward path allocates device memory or
+ *     synchronises.
+ *   - Ownership: the caller owns every activation, id, logits, KV cache and
+ *     workspace buffer.  The model (tp_model) owns only the weight shards, a
+ *     RoPE table and a small device status word, all freed by tp_free.
+ *   - Errors: argument and rule violations are returned before anything is
+ *     launched.  Errors found on the device (a token id >= vocab, a pipeline
+ *     wait that ran out) set the model's device status word; tp_check_device
+ *     reads and clears it.  No call aborts the process or throws.
+ *   - Workspace: calls that take (ws, ws_bytes) need at least
+ *     tp_workspace_bytes(model, M) bytes, zero-filled before the first use
+ *     (tp_workspace_init).  The kernels leave the counters in it at zero when
+ *     they finish; after a device error, zero it again.  Calls that use the
+ *     same workspace must not overlap on the device.
+ */
+#ifndef TP_GB300_H
+#define TP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t tp_bf16; /* bit pattern of one bfloat16 value */
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_ARG = 1,            /* null pointer, bad index, size out of range */
+  TP_ERR_DIVISIBILITY = 2,   /* n_heads % t, intermediate % t, n_heads % n_kv_heads */
+  TP_ERR_KV_REPLICA = 3,     /* n_kv >= t with n_kv % t != 0, or n_kv < t with t % n_kv != 0 */
+  TP_ERR_TOKEN_RANGE = 4,    /* (device) a token id outside [0, vocab) */
+  TP_ERR_OOM = 5,            /* device allocation failed in tp_load_shards */
+  TP_ERR_CUDA = 6,           /* a CUDA runtime call failed */
+  TP_ERR_DEVICE_TIMEOUT = 7, /* (device) a bounded pipeline wait ran out */
+  TP_ERR_UNSUPPORTED = 8,    /* shape outside the kernels' envelope (see tp_config) */
+  TP_ERR_WORKSPACE = 9       /* workspace missing or smaller than tp_workspace_bytes */
+} tp_status;
+
+/* Model shape.  The caller fills the first block; tp_config validates it and
+ * fills the derived block.
+ *
+ * Rules (P1 §3.2 切分): Q heads split by head, so n_heads % t == 0.  KV heads
+ * split n_kv/t per rank when n_kv >= t (n_kv % t == 0); when n_kv < t each KV
+ * head is replicated on t/n_kv ranks that share one cache copy
+ * (t % n_kv == 0), and rank r reads KV head r / (t/n_kv).  The vocabulary is
+ * padded to a multiple of t with zero rows and split evenly.  The
+ * intermediate size splits evenly (intermediate % t == 0).
+ *
+ * Kernel envelope (TP_ERR_UNSUPPORTED otherwise): head_dim in {64, 128};
+ * hidden, n_heads*head_dim/t and intermediate/t multiples of 64;
+ * 1 <= t <= 8; max_positions >= 1. */
+typedef struct {
+  int32_t hidden;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t intermediate;
+  int32_t vocab;
+  int32_t n_layers;
+  int32_t t;             /* emulated TP ranks */
+  float rms_eps;         /* RMSNorm epsilon */
+  float rope_theta;      /* RoPE base */
+  int32_t max_positions; /* RoPE table length: every position must be < this */
+  /* derived, written by tp_config */
+  int32_t vocab_padded;
+  int32_t vocab_per_rank;
+  int32_t q_heads_per_rank;
+  int32_t kv_heads_per_rank; /* KV heads in one rank's cache (1 when replicated) */
+  int32_t kv_replicas;       /* ranks sharing one KV head (1 when split) */
+  int32_t kv_copies;         /* distinct per-rank caches = min(t, n_kv_heads) */
+  int32_t inter_per_rank;
+} tp_config_t;
+
+/* Validates the shape and fills the derived fields. */
+tp_status tp_config(tp_config_t* c);
+
+/* Unsharded weights of one decoder layer (device pointers, bf16).
+ * attn_norm, mlp_norm [H]; wq [n_heads*d, H]; wk, wv [n_kv*d, H];
+ * wo [H, n_heads*d]; wg, wu [I, H]; wd [H, I]. */
+typedef struct {
+  const tp_bf16 *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
+} tp_layer_weights_t;
+
+/* embed, lm_head [vocab, H]; final_norm [H]: may all be NULL for a model used
+ * layer by layer.  `layers` is a HOST array of n_layers entries. */
+typedef struct {
+  const tp_bf16* embed;
+  const tp_bf16* final_norm;
+  const tp_bf16* lm_head;
+  const tp_layer_weights_t* layers;
+} tp_weights_t;
+
+typedef struct tp_model tp_model; /* opaque: owns the shard buffers */
+
+/* Builds the t per-rank shards (P1 §3.2 切分; P3 线性层怎么切) on the device of
+ * the current CUDA context and returns the model.  The unsharded weights are
+ * only read; the caller may free them afterwards.  Synchronises `stream`.
+ *   qkv shard r    : rows of rank r's Q heads, then of its KV heads (copies
+ *                    when replicated) — column-parallel
+ *   gate_up shard r: rows [r I/t, (r+1) I/t) of the gate and of the up weight
+ *                    — column-parallel
+ *   o / down shard r: columns [r K/t, (r+1) K/t) of wo / wd — row-parallel
+ *   embed / lm_head shard r: vocab rows [r Vp/t, (r+1) Vp/t), zero padded
+ * Within a shard, rows are stored in the order the fused epilogues want (the
+ * two halves of each RoPE pair, and each gate row with its up row, sit next
+ * to each other); every output of the API is in the standard order. */
+tp_status tp_load_shards(const tp_config_t* cfg, const tp_weights_t* w, void* stream,
+                         tp_model** out);
+void tp_free(tp_model* m);
+tp_status tp_get_config(const tp_model* m, tp_config_t* out);
+
+/* Workspace bytes needed by any call on up to max_tokens rows. */
+size_t tp_workspace_bytes(const tp_model* m, int32_t max_tokens);
+/* Zero-fills a workspace (async on stream). */
+tp_status tp_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+enum { TP_QKV = 0, TP_GATE_UP = 1, TP_O = 2, TP_DOWN = 3 };
+
+/* Column-parallel linear, all t ranks in one launch (P3 线性层怎么切: the
+ * weight A is split along the output dimension, rank i computes
+ * Y_i = X A_i from the full replicated X, and the outputs stay sharded —
+ * no communication, gather_output = false).
+ *   which : TP_QKV or TP_GATE_UP
+ *   x     : [M, H] bf16
+ *   y     : rank r's output at y + r*y_rank_stride (elements), [M, N_r]
+ *           row-major with N_r = (q_heads_per_rank + 2 kv_heads_per_rank)*d
+ *           for TP_QKV (its Q heads, then K heads, then V heads) and
+ *           N_r = 2 I/t for TP_GATE_UP (gate slice, then up slice).
+ *           y_rank_stride >= M*N_r.
+ * Plain GEMM output: no RoPE, no activation. */
+tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
+                           int32_t M, tp_bf16* y, int64_t y_rank_stride, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Row-parallel linear plus the all-reduce of its t partial sums
+ * (P1 §3.1: Y = Y_0 + Y_1 + ... + Y_{t-1}; P3 线性层怎么切).
+ *   which    : TP_O or TP_DOWN
+ *   x        : rank r's input shard at x + r*x_rank_stride, [M, K_r] with row
+ *              stride ldx (K_r = n_heads*d/t for TP_O, I/t for TP_DOWN)
+ *   residual : [M, H] or NULL; added once, in fp32, before the rounding
+ *   y        : [M, H] bf16; may alias `residual`
+ *   fused    : 1 = one kernel; the t partials are accumulated in fp32 in
+ *              rank order 0..t-1 and rounded once to bf16 in its epilogue.
+ *              0 = each rank's fp32 partial is written to the workspace, then
+ *              a separate kernel sums them in rank order (same rounding).
+ * The reduction order is fixed, so results are deterministic. */
+tp_status tp_row_linear_reduce(const tp_model* m, int32_t layer, int32_t which,
+                               const tp_bf16* x, int64_t x_rank_stride, int64_t ldx, int32_t M,
+                               const tp_bf16* residual, tp_bf16* y, int32_t fused, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Vocab-parallel embedding (P1 §3.2 Vocab Parallel; P3 词嵌入): rank r looks
+ * up only ids in [r Vp/t, (r+1) Vp/t) and contributes -0.0 elsewhere; the t
+ * contributions are summed in rank order, which reproduces E[id] bit for bit.
+ *   ids : [M] int32;  h : [M, H] bf16.
+ * An id outside [0, vocab) writes a zero row and sets TP_ERR_TOKEN_RANGE in
+ * the device status word. */
+tp_status tp_vocab_embed(const tp_model* m, const int32_t* ids, int32_t M, tp_bf16* h,
+                         void* stream);
+
+/* Vocab-parallel LM head with the logits all-gather (P1 §3.1 All-Gather:
+ * Y = cat(Y_0, ..., Y_{t-1}); P3 输出层).  Rank r computes logits of its
+ * Vp/t vocab rows and writes them straight into columns [r Vp/t, (r+1) Vp/t)
+ * of the output; columns >= vocab (padding) are not written.
+ *   x      : [S, H] bf16 (already normalised)
+ *   logits : [S, vocab] bf16 with row stride ld_logits >= vocab */
+tp_status tp_lm_head_gather(const tp_model* m, const tp_bf16* x, int32_t S, tp_bf16* logits,
+                            int64_t ld_logits, void* ws, size_t ws_bytes, void* stream);
+
+enum { TP_DECODE = 0, TP_PREFILL = 1 };
+
+/* One forward step's batch.
+ * Tokens are grouped by sequence: sequence b owns tokens
+ * [seq_start[b], seq_start[b+1]).  Token i sits at position positions[i] of
+ * its sequence and attends to cache positions 0..positions[i] of that
+ * sequence (causal).  In DECODE mode token b is the single token of sequence
+ * b (seq_start may be NULL).
+ * KV cache (per layer, caller-owned, bf16): rank copy c of sequence b, KV head
+ * g (local to the copy), position p, element e lives at
+ *   base[(((c*n_seqs + b)*kv_heads_per_rank + g)*l_max + p)*head_dim + e]
+ * Replica ranks (n_kv < t) share copy c = r / kv_replicas.  The layer writes
+ * each token's K and V at its position before attention reads them. */
+typedef struct {
+  int32_t mode;                /* TP_DECODE or TP_PREFILL */
+  int32_t n_seqs;
+  int32_t n_tokens;            /* M */
+  int32_t max_q_per_seq;       /* host: max tokens of one sequence in this batch */
+  int32_t max_ctx;             /* host: max over tokens of positions[i] + 1 */
+  int32_t l_max;               /* cache capacity per sequence (positions < l_max) */
+  const int32_t* seq_start;    /* device [n_seqs + 1] (PREFILL) */
+  const int32_t* positions;    /* device [n_tokens] */
+  const int32_t* token_seq;    /* device [n_tokens]: sequence of each token */
+  tp_bf16* const* k_cache;     /* HOST array [n_layers] of device base pointers */
+  tp_bf16* const* v_cache;     /* HOST array [n_layers] of device base pointers */
+  const int32_t* sample_rows;  /* device [n_samples]: token rows that produce logits */
+  int32_t n_samples;
+} tp_batch_t;
+
+/* One decoder layer, all t ranks (P3 线性层怎么切 flowchart; P2 前向执行的实际流程):
+ *   u = RMSNorm(h)                        replicated
+ *   q,k,v = column-parallel qkv_proj(u), RoPE on q and k, k/v -> rank caches
+ *   o = per-rank GQA attention over the rank's own heads and cache
+ *   h = h + all_reduce(row-parallel o_proj(o))           reduction ①
+ *   u = RMSNorm(h)
+ *   a = SiLU(gate) * up from column-parallel gate_up_proj(u)
+ *   h = h + all_reduce(row-parallel down_proj(a))        reduction ②
+ * h_inout [n_tokens, H] bf16 is read and overwritten.  fused selects the
+ * row-parallel reduction variant (see tp_row_linear_reduce). */
+tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                           tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Full forward: vocab-parallel embedding of ids [n_tokens] into h, every
+ * layer, final RMSNorm of the sampled rows, vocab-parallel LM head gathered
+ * into logits [n_samples, vocab] (row stride ld_logits).
+ *   h : [n_tokens, H] bf16 scratch that ends holding the last hidden state. */
+tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
+                     tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* Replicated RMSNorm (P1 §3.2: small layers stay whole on every rank):
+ * y = x / sqrt(mean(x^2) + eps) * w, fp32 arithmetic, bf16 in and out.
+ *   x, y : [M, H] (may alias); w : [H] — any device vector. */
+tp_status tp_rmsnorm(const tp_model* m, const tp_bf16* x, const tp_bf16* w, int32_t M,
+                     tp_bf16* y, void* stream);
+
+/* Counters of the emulated collectives, accumulated by the host over every
+ * launch since the model was created (or tp_reset_stats).  The payload is the
+ * bf16 result each all-reduce delivers (M*H*2 bytes) and, for the gather, the
+ * bytes of the concatenated logits each rank receives from the others
+ * ((t-1)/t * vocab * 2 bytes per sampled row) (P3 每 token 的通信量). */
+typedef struct {
+  int64_t allreduces;          /* row-parallel reductions + embedding reductions */
+  int64_t allreduce_payload_bytes;
+  int64_t allgathers;          /* logits gathers */
+  int64_t allgather_recv_bytes_per_rank;
+  int64_t kernel_launches;     /* kernels launched by the library */
+} tp_stats_t;
+
+tp_status tp_get_stats(const tp_model* m, tp_stats_t* out);
+void tp_reset_stats(tp_model* m);
+
+/* Synchronises `stream`, returns the device status word (TP_OK,
+ * TP_ERR_TOKEN_RANGE or TP_ERR_DEVICE_TIMEOUT) and clears it. */
+tp_status tp_check_device(tp_model* m, void* stream);
+
+const char* tp_strerror(tp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TP_GB300_H */

@@ -1,0 +1,574 @@
+// Head-sharded GQA attention over the per-rank KV caches ("Tensor Parallelism
+// 执行路径", KV Cache 在 TP 下怎样分布: rank i stores and reads only the K/V of
+// its own heads; "张量、流水线与数据并行", 线性层怎么切: attention on each rank's own
+// heads with its own KV).
+//
+// All t ranks run in one launch.  Rank r owns Q heads [r n_h/t, (r+1) n_h/t),
+// which in the concatenated q/o buffers is simply the global head order, and
+// Q head j reads KV head g = j / (n_h/n_kv).  KV head g lives in rank copy
+// g / kv_r at local index g % kv_r; replica ranks (n_kv < t) share that copy,
+// so one CTA serves every Q head of KV head g and reads its K/V once.
+//
+// K/V tiles of 64 positions arrive by TMA (128-byte swizzle) and feed
+// mma.sync tiles from ldmatrix; scores and the online softmax stay in fp32.
+//   decode : one query token per sequence; the (sequence, KV head, key tile)
+//            space is split evenly over a persistent grid ("stream-K"); pieces
+//            of one (sequence, KV head) are combined in key order by the last
+//            CTA to finish one (atomic ticket, no waiting).
+//   prefill: causal; one CTA per (sequence, Q head, 64-token query block).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpk {
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 8-element chunk `ch` of row `row` in a K/V tile made of
+// D/64 TMA boxes of [64 rows][128 B] with 128-byte swizzle.
+__device__ __forceinline__ uint32_t kv_off(int row, int ch) {
+  return (ch >> 3) * 8192 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+}
+
+constexpr int kKeyTile = 64;
+
+// One warp: scores of 16 query rows against 64 keys, then the online-softmax
+// update of (m, l, O).  qa: Q A-fragments; sK/sV: smem tiles.  key0: position
+// of the first key; lim[2]: last visible key position (inclusive) of the
+// thread's two rows.
+template <int D>
+__device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint32_t sK,
+                                          uint32_t sV, int key0, const int (&lim)[2],
+                                          float scale_log2, float (&m)[2], float (&l)[2],
+                                          float (&o)[D / 8][4]) {
+  const int lane = threadIdx.x & 31;
+  float s[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {  // pairs of 8-key n-tiles
+      const int j = lane >> 3, r = lane & 7;
+      const int key = (np * 2 + (j >> 1)) * 8 + r;
+      const int ch = kk * 2 + (j & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sK + kv_off(key, ch), b0, b1, b2, b3);
+      mma_16816(s[np * 2], qa[kk], b0, b1);
+      mma_16816(s[np * 2 + 1], qa[kk], b2, b3);
+    }
+  }
+  // mask + tile row max
+  float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = key0 + nt * 8 + (lane & 3) * 2 + (i & 1);
+      const int h = i >> 1;
+      float v = s[nt][i] * scale_log2;
+      v = key <= lim[h] ? v : -INFINITY;
+      s[nt][i] = v;
+      tmax[h] = fmaxf(tmax[h], v);
+    }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+    tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+  }
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    mnew[h] = fmaxf(m[h], tmax[h]);
+    alpha[h] = (mnew[h] == -INFINITY) ? 1.f : exp2f(m[h] - mnew[h]);
+    m[h] = mnew[h];
+    l[h] *= alpha[h];
+  }
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) {
+    o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
+    o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+  }
+  uint32_t pa[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int h = i >> 1;
+      p[i] = (mnew[h] == -INFINITY) ? 0.f : exp2f(s[nt][i] - mnew[h]);
+      l[h] += p[i];
+    }
+    pa[nt >> 1][(nt & 1) * 2 + 0] = pack2(p[0], p[1]);
+    pa[nt >> 1][(nt & 1) * 2 + 1] = pack2(p[2], p[3]);
+  }
+  // O += P V
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+    for (int np = 0; np < D / 16; ++np) {
+      const int j = lane >> 3, r = lane & 7;
+      const int key = kk * 16 + (j & 1) * 8 + r;
+      const int ch = np * 2 + (j >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sV + kv_off(key, ch), b0, b1, b2, b3);
+      mma_16816(o[np * 2], pa[kk], b0, b1);
+      mma_16816(o[np * 2 + 1], pa[kk], b2, b3);
+    }
+  }
+}
+
+// Loads the A fragments of 16 query rows from a padded smem block.
+template <int D>
+__device__ __forceinline__ void load_q_frags(uint32_t sQ, int row_bytes, uint32_t (&qa)[D / 16][4]) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 3, r = lane & 7;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int row = r + (j & 1) * 8;
+    const int col = kk * 16 + (j >> 1) * 8;
+    ldsm_x4(sQ + row * row_bytes + col * 2, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  }
+}
+
+// ============================================================================
+// decode
+// ============================================================================
+constexpr int kDecWarps = 4;                       // compute warps
+constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + producer warp
+
+template <int D>
+struct DecSmem {
+  static constexpr int kTileBytes = (D / 64) * 8192;       // one K or V tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQRow = D * 2 + 16;                 // padded bf16 row
+  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kComb = kDecWarps * 16 * (D + 2);   // floats: O, m, l per warp/row
+  static constexpr size_t bytes(int) {
+    return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
+  using L = DecSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint8_t* sQ = tiles + L::kStages * L::kStageBytes;
+  float* comb = reinterpret_cast<float*>(sQ + 16 * L::kQRow);
+  uint64_t* full = reinterpret_cast<uint64_t*>(comb + L::kComb);
+  uint64_t* empty = full + L::kStages;
+  int* last_flag = reinterpret_cast<int*>(empty + L::kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = L::kStages;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  const int G = a.grid, c = blockIdx.x;
+  const int64_t T = a.total_units;
+  const int TB = a.tiles_per_bg;
+  const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
+
+  if (warp == kDecWarps) {
+    // producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tmK);
+      tma_prefetch_desc(&a.tmV);
+      const uint64_t pol = policy_evict_first();
+      uint32_t n = 0;
+      for (int64_t u = beg; u < end; ++u) {
+        const int64_t bg = u / TB;
+        const int tile = static_cast<int>(u - bg * TB);
+        const int b = static_cast<int>(bg / a.n_kv), g = static_cast<int>(bg % a.n_kv);
+        const int slice = ((g / a.kv_r) * a.n_seqs + b) * a.kv_r + (g % a.kv_r);
+        const uint32_t s = n % S, ph = (n / S) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
+        mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+        uint8_t* kt = tiles + s * L::kStageBytes;
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_3d(kt + bx * 8192, &a.tmK, &full[s], bx * 64, tile * kKeyTile, slice, pol);
+          tma_load_3d(kt + L::kTileBytes + bx * 8192, &a.tmV, &full[s], bx * 64, tile * kKeyTile,
+                      slice, pol);
+        }
+        ++n;
+      }
+      for (uint32_t i = (n > (uint32_t)S ? n - S : 0); i < n; ++i)
+        mbar_wait(&full[i % S], (i / S) & 1, a.status);
+    }
+  } else {
+    const int ctid = threadIdx.x;  // 0..127
+    uint32_t n_base = 0;           // CTA-local index of the segment's first unit
+    bool alive = true;
+    for (int64_t u0 = beg; u0 < end;) {
+      const int64_t bg = u0 / TB;
+      const int64_t seg_end = min(end, (bg + 1) * TB);
+      const int len = static_cast<int>(seg_end - u0);
+      const int tile0 = static_cast<int>(u0 - bg * TB);
+      const int b = static_cast<int>(bg / a.n_kv), g = static_cast<int>(bg % a.n_kv);
+      const int pos = a.positions[b];
+      // stage the group's query rows (16 rows, zero beyond the group)
+      for (int i = ctid; i < 16 * (D / 8); i += kDecWarps * 32) {
+        const int row = i / (D / 8), ch = i % (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < a.group)
+          v = *reinterpret_cast<const uint4*>(a.q + (int64_t)b * a.ld_q +
+                                              (int64_t)(g * a.group + row) * D + ch * 8);
+        *reinterpret_cast<uint4*>(sQ + row * L::kQRow + ch * 16) = v;
+      }
+      bar_sync(1, kDecWarps * 32);
+      uint32_t qa[D / 16][4];
+      load_q_frags<D>(smem_u32(sQ), L::kQRow, qa);
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      float o[D / 8][4];
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
+      const int lim[2] = {pos, pos};
+      for (int i = warp; i < len; i += kDecWarps) {
+        const uint32_t n = n_base + i;
+        const uint32_t s = n % S, ph = (n / S) & 1;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&full[s], ph, a.status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) { alive = false; break; }
+        const int key0 = (tile0 + i) * kKeyTile;
+        if (key0 <= pos) {
+          const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
+          attn_tile<D>(qa, st, st + L::kTileBytes, key0, lim, a.scale_log2, m, l, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      n_base += len;
+      // combine the 4 warps' (m, l, O) in smem
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+      }
+      float* cw = comb + warp * 16 * (D + 2);
+      const int r0 = lane >> 2;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt) {
+        const int col = nt * 8 + (lane & 3) * 2;
+        cw[r0 * (D + 2) + col] = o[nt][0];
+        cw[r0 * (D + 2) + col + 1] = o[nt][1];
+        cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
+        cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
+      }
+      if ((lane & 3) == 0) {
+        cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
+        cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
+      }
+      const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
+      // 128 threads: row = ctid / 8, 16 columns each (D = 128) or 8 (D = 64)
+      constexpr int CPT = D / 8;
+      const int row = ctid >> 3, c0 = (ctid & 7) * CPT;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
+      float ll = 0.f, acc[CPT];
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float* cr = comb + (w * 16 + row) * (D + 2);
+        const float mw = cr[D];
+        if (mw == -INFINITY) continue;
+        const float sc = exp2f(mw - mm);
+        ll += cr[D + 1] * sc;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) acc[j] += cr[c0 + j] * sc;
+      }
+      const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
+      uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + c0;
+      if (nseg == 1) {
+        if (row < a.group) {
+          const float inv = 1.f / ll;
+#pragma unroll
+          for (int j = 0; j < CPT; j += 8) {
+            uint4 v;
+            uint32_t* p = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) p[q] = pack2(acc[j + 2 * q] * inv, acc[j + 2 * q + 1] * inv);
+            *reinterpret_cast<uint4*>(orow + j) = v;
+          }
+        }
+      } else {
+        const int first_c = owner_of(bg * TB, T, G);
+        const int my_slot = (beg / TB == bg) ? 0 : 1;
+        float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
+        if ((ctid & 7) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
+        __threadfence();
+        bar_sync(1, kDecWarps * 32);
+        if (ctid == 0) {
+          const int old = atomicAdd(&a.tickets[bg], 1);
+          *last_flag = (old == nseg - 1) ? 1 : 0;
+        }
+        bar_sync(1, kDecWarps * 32);
+        if (*last_flag) {
+          __threadfence();
+          float M2 = -INFINITY;
+          for (int sgi = 0; sgi < nseg; ++sgi) {
+            const int cc = first_c + sgi;
+            const int slot = (range_begin(cc, T, G) / TB == bg) ? 0 : 1;
+            const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
+            M2 = fmaxf(M2, __ldcg(&src[row * (D + 2) + D]));
+          }
+          float L2 = 0.f, acc2[CPT];
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) acc2[j] = 0.f;
+          for (int sgi = 0; sgi < nseg; ++sgi) {
+            const int cc = first_c + sgi;
+            const int slot = (range_begin(cc, T, G) / TB == bg) ? 0 : 1;
+            const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
+            const float ms = __ldcg(&src[row * (D + 2) + D]);
+            if (ms == -INFINITY) continue;
+            const float sc = exp2f(ms - M2);
+            L2 += __ldcg(&src[row * (D + 2) + D + 1]) * sc;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + c0 + j]) * sc;
+          }
+          if (row < a.group) {
+            const float inv = 1.f / L2;
+#pragma unroll
+            for (int j = 0; j < CPT; j += 8) {
+              uint4 v;
+              uint32_t* p = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                p[q] = pack2(acc2[j + 2 * q] * inv, acc2[j + 2 * q + 1] * inv);
+              *reinterpret_cast<uint4*>(orow + j) = v;
+            }
+          }
+          if (ctid == 0) a.tickets[bg] = 0;
+        }
+      }
+      bar_sync(1, kDecWarps * 32);  // smem (q, comb, flag) reused by the next segment
+      if (any_dead) break;
+      u0 = seg_end;
+    }
+  }
+  __syncthreads();
+}
+
+// ============================================================================
+// prefill (causal within each sequence)
+// ============================================================================
+constexpr int kPreThreads = 128;
+constexpr int kPreStages = 2;
+
+template <int D>
+struct PreSmem {
+  static constexpr int kTileBytes = (D / 64) * 8192;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQRow = D * 2 + 16;
+  static constexpr size_t bytes() {
+    return 1024 + (size_t)kPreStages * kStageBytes + 64 * kQRow + 128;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_constant__ AttnArgs a) {
+  using L = PreSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint8_t* sQ = tiles + kPreStages * L::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + 64 * L::kQRow);
+  int* flags = reinterpret_cast<int*>(full + kPreStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int n_qb = gridDim.x;
+  const int qb = n_qb - 1 - blockIdx.x;  // longest blocks first
+  const int t0 = a.seq_start[b], t1 = a.seq_start[b + 1];
+  const int q0 = t0 + qb * 64;
+  if (q0 >= t1) return;
+  const int nrows = min(64, t1 - q0);
+  const int g = h / a.group;
+  const int slice = ((g / a.kv_r) * a.n_seqs + b) * a.kv_r + (g % a.kv_r);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPreStages; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    int mx = 0;
+    for (int i = 0; i < nrows; ++i) mx = max(mx, a.positions[q0 + i]);
+    flags[0] = mx;
+  }
+  // stage q rows
+  for (int i = threadIdx.x; i < 64 * (D / 8); i += kPreThreads) {
+    const int row = i / (D / 8), ch = i % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < nrows) v = *reinterpret_cast<const uint4*>(a.q + (int64_t)(q0 + row) * a.ld_q + (int64_t)h * D + ch * 8);
+    *reinterpret_cast<uint4*>(sQ + row * L::kQRow + ch * 16) = v;
+  }
+  __syncthreads();
+  const int max_pos = min(flags[0], a.l_max - 1);
+  const int n_tiles = max_pos / kKeyTile + 1;
+  const uint64_t pol = policy_evict_last();
+  auto issue = [&](int tile) {
+    const int s = tile % kPreStages;
+    uint8_t* kt = tiles + s * L::kStageBytes;
+    mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx) {
+      tma_load_3d(kt + bx * 8192, &a.tmK, &full[s], bx * 64, tile * kKeyTile, slice, pol);
+      tma_load_3d(kt + L::kTileBytes + bx * 8192, &a.tmV, &full[s], bx * 64, tile * kKeyTile, slice, pol);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(kPreStages, n_tiles); ++i) issue(i);
+
+  uint32_t qa[D / 16][4];
+  load_q_frags<D>(smem_u32(sQ) + warp * 16 * L::kQRow, L::kQRow, qa);
+  const int r0 = warp * 16 + (lane >> 2);
+  int lim[2];
+  lim[0] = r0 < nrows ? a.positions[q0 + r0] : -1;
+  lim[1] = r0 + 8 < nrows ? a.positions[q0 + r0 + 8] : -1;
+  int warp_max = max(lim[0], lim[1]);
+  warp_max = max(warp_max, __shfl_xor_sync(0xffffffffu, warp_max, 4));
+  warp_max = max(warp_max, __shfl_xor_sync(0xffffffffu, warp_max, 8));
+  warp_max = max(warp_max, __shfl_xor_sync(0xffffffffu, warp_max, 16));
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[D / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
+
+  bool alive = true;
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int s = tile % kPreStages;
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(&full[s], (tile / kPreStages) & 1, a.status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    const bool dead = __syncthreads_or(!ok);
+    if (dead) { alive = false; break; }
+    const int key0 = tile * kKeyTile;
+    if (key0 <= warp_max) {
+      const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
+      attn_tile<D>(qa, st, st + L::kTileBytes, key0, lim, a.scale_log2, m, l, o);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && tile + kPreStages < n_tiles) issue(tile + kPreStages);
+  }
+  if (!alive) {
+    // let copies in flight land before the CTA exits
+    if (threadIdx.x == 0)
+      for (int tile = 0; tile < n_tiles; ++tile)
+        mbar_wait(&full[tile % kPreStages], (tile / kPreStages) & 1, a.status);
+    __syncthreads();
+    return;
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
+    l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int row = r0 + hh * 8;
+    if (row >= nrows) continue;
+    const float inv = 1.f / l[hh];
+    uint16_t* orow = a.o + (int64_t)(q0 + row) * a.ld_o + (int64_t)h * D;
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      const int col = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<uint32_t*>(orow + col) = pack2(o[nt][hh * 2] * inv, o[nt][hh * 2 + 1] * inv);
+    }
+  }
+}
+
+// ============================================================================
+// host launchers
+// ============================================================================
+template <int D>
+static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
+  const size_t smem = DecSmem<D>::bytes(0);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  attn_decode_kernel<D><<<a.grid, kDecThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_prefill_t(const AttnArgs& a, int n_qb, cudaStream_t st) {
+  const size_t smem = PreSmem<D>::bytes();
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(n_qb, a.n_heads, a.n_seqs);
+  attn_prefill_kernel<D><<<grid, kPreThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {
+  return a.head_dim == 128 ? launch_decode_t<128>(a, st) : launch_decode_t<64>(a, st);
+}
+
+cudaError_t launch_attn_prefill(const AttnArgs& a, int n_qb, cudaStream_t st) {
+  return a.head_dim == 128 ? launch_prefill_t<128>(a, n_qb, st) : launch_prefill_t<64>(a, n_qb, st);
+}
+
+size_t attn_decode_partial_floats(int head_dim) { return 16 * (size_t)(head_dim + 2); }
+
+}  // namespace tpk
+
+namespace tpk {
+size_t attn_decode_smem_bytes(int head_dim) {
+  return head_dim == 128 ? DecSmem<128>::bytes(0) : DecSmem<64>::bytes(0);
+}
+}  // namespace tpk

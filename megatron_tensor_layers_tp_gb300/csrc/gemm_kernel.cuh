@@ -1,0 +1,480 @@
+// Sharded GEMM on the 5th-generation tensor cores: D = A * B^T, both operands
+// K-major bf16 fed by TMA (128-byte swizzle), fp32 accumulators in tensor
+// memory, fused epilogues for the tensor-parallel layer.
+//
+// One launch covers all t emulated ranks.  Operands are 3-D tensor maps
+// (K, rows, slice) where the slice coordinate is the rank shard.  Work is the
+// flat sequence of (output tile, 64-wide K step) pairs; CTA c of G processes
+// the contiguous range [c*T/G, (c+1)*T/G) ("stream-K"), so every CTA streams
+// the same number of bytes.  A tile cut between CTAs leaves fp32 partials in
+// the workspace; the last CTA to finish a piece of the tile (atomic ticket, no
+// waiting) adds the pieces in K order — which is rank order for the fused
+// row-parallel reduction — and runs the epilogue.  The result is deterministic
+// for a given grid.
+//
+// Roles (192 threads): warp 0 issues TMA loads, warp 1 issues tcgen05.mma from
+// one thread into one of two TMEM accumulators, warps 2..5 drain the other
+// accumulator (tcgen05.ld) and run the epilogue.  Every wait is bounded.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpk {
+
+constexpr int kThreads = 192;
+constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
+
+__device__ __forceinline__ uint64_t make_policy(int kind) {
+  if (kind == 1) return policy_evict_first();
+  if (kind == 2) return policy_evict_last();
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ int slice_of(int mode, int g, int ks) {
+  return mode == 1 ? g : (mode == 2 ? ks : 0);
+}
+
+// --------------------------------------------------------------------------
+// epilogues: one call handles 16 accumulator columns of one TMEM lane.
+// SWAP (decode): lane = feature row of the weight, columns = tokens.
+// !SWAP (prefill): lane = token, columns = feature rows.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void qkv_classify(const EpiArgs& e, int f, int& kind, int& head,
+                                             int& w) {
+  const int d = e.head_dim;
+  const int nq = e.q_heads_per_rank * d, nk = e.kv_heads_per_rank * d;
+  if (f < nq) { kind = 0; head = f / d; w = f - head * d; }
+  else if (f < nq + nk) { kind = 1; head = (f - nq) / d; w = f - nq - head * d; }
+  else { kind = 2; head = (f - nq - nk) / d; w = f - nq - nk - head * d; }
+}
+
+// Standard per-rank column of shard row f (undoes the pair interleaving).
+__device__ __forceinline__ int plain_col(const EpiArgs& e, int f) {
+  if (e.which == 1) return (f & 1) ? e.inter_per_rank + (f >> 1) : (f >> 1);
+  int kind, head, w;
+  qkv_classify(e, f, kind, head, w);
+  const int d = e.head_dim;
+  const int base = f - w;
+  if (kind == 2) return f;
+  return base + ((w & 1) ? (w >> 1) + d / 2 : (w >> 1));
+}
+
+template <bool SWAP, int EPI>
+__device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
+                                          float (&v)[16]) {
+  const EpiArgs& e = a.e;
+  if constexpr (SWAP) {
+    const int f = arow;
+    const bool fval = f < a.a_rows_valid;
+    if constexpr (EPI == EPI_RESID) {
+      uint16_t* out = static_cast<uint16_t*>(e.out);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        if (fval && m < e.M) {
+          float r = e.residual ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f]) : 0.f;
+          out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + r);
+        }
+      }
+    } else if constexpr (EPI == EPI_PARTIAL) {
+      float* out = static_cast<float*>(e.out) + (int64_t)g * e.out_group_stride;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = v[j];
+      }
+    } else if constexpr (EPI == EPI_PLAIN) {
+      uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)g * e.out_group_stride;
+      const int col = fval ? plain_col(e, f) : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        if (fval && m < e.M) out[(int64_t)m * e.ld_out + col] = f_to_bf16(v[j]);
+      }
+    } else if constexpr (EPI == EPI_LOGITS) {
+      uint16_t* out = static_cast<uint16_t*>(e.out);
+      const int64_t col = (int64_t)g * e.vocab_per_rank + f;
+      const bool ok = fval && f < e.vocab_per_rank && col < e.vocab;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        if (ok && m < e.M) out[(int64_t)m * e.ld_out + col] = f_to_bf16(v[j]);
+      }
+    } else if constexpr (EPI == EPI_SILU) {
+      uint16_t* out = static_cast<uint16_t*>(e.out);
+      const int64_t col = (int64_t)g * e.inter_per_rank + (f >> 1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        const int m = brow0 + j;
+        if (fval && !(f & 1) && m < e.M) {
+          const float gt = v[j], up = partner;
+          out[(int64_t)m * e.ld_out + col] = f_to_bf16(gt / (1.f + expf(-gt)) * up);
+        }
+      }
+    } else if constexpr (EPI == EPI_QKV) {
+      int kind = 2, head = 0, w = 0;
+      if (fval) qkv_classify(e, f, kind, head, w);
+      const int d = e.head_dim, half = d / 2;
+      const int jp = w >> 1;
+      const bool second = (w & 1) != 0;
+      const int feat = kind == 2 ? w : (second ? jp + half : jp);
+      const bool primary = (g % e.kv_replicas) == 0;
+      const int copy = g / e.kv_replicas;
+      uint16_t* qout = static_cast<uint16_t*>(e.out);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        const int m = brow0 + j;
+        if (!fval || m >= e.M) continue;
+        const int pos = e.positions[m];
+        if (pos < 0 || pos >= e.l_max) continue;  // never index the cache or table out of range
+        float val = v[j];
+        if (kind != 2) {
+          const float2 cs = e.rope[(int64_t)pos * half + jp];
+          val = second ? (v[j] * cs.x + partner * cs.y) : (v[j] * cs.x - partner * cs.y);
+        }
+        if (kind == 0) {
+          qout[(int64_t)m * e.ld_out + (int64_t)(g * e.q_heads_per_rank + head) * d + feat] =
+              f_to_bf16(val);
+        } else if (primary) {
+          const int seq = e.token_seq[m];
+          uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
+          const int64_t idx = copy * e.kv_copy_stride +
+                              (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d + feat;
+          cache[idx] = f_to_bf16(val);
+        }
+      }
+    }
+  } else {
+    const int m = arow;
+    const int f0 = brow0;
+    if (m >= e.M || f0 >= a.b_rows_valid) return;
+    if constexpr (EPI == EPI_RESID) {
+      uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out + f0;
+      float r[16];
+      if (e.residual) {
+        const uint4* rp = reinterpret_cast<const uint4*>(e.residual + (int64_t)m * e.ld_res + f0);
+        uint4 r0 = rp[0], r1 = rp[1];
+        const uint16_t* rb0 = reinterpret_cast<const uint16_t*>(&r0);
+        const uint16_t* rb1 = reinterpret_cast<const uint16_t*>(&r1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { r[j] = bf16_to_f(rb0[j]); r[8 + j] = bf16_to_f(rb1[j]); }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = 0.f;
+      }
+      uint4 o0, o1;
+      uint32_t* p0 = reinterpret_cast<uint32_t*>(&o0);
+      uint32_t* p1 = reinterpret_cast<uint32_t*>(&o1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        p0[j] = pack_bf16x2(v[2 * j] + r[2 * j], v[2 * j + 1] + r[2 * j + 1]);
+        p1[j] = pack_bf16x2(v[8 + 2 * j] + r[8 + 2 * j], v[9 + 2 * j] + r[9 + 2 * j]);
+      }
+      reinterpret_cast<uint4*>(out)[0] = o0;
+      reinterpret_cast<uint4*>(out)[1] = o1;
+    } else if constexpr (EPI == EPI_PARTIAL) {
+      float4* out = reinterpret_cast<float4*>(static_cast<float*>(e.out) +
+                                              (int64_t)g * e.out_group_stride +
+                                              (int64_t)m * e.ld_out + f0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) out[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else if constexpr (EPI == EPI_PLAIN) {
+      uint16_t* row = static_cast<uint16_t*>(e.out) + (int64_t)g * e.out_group_stride +
+                      (int64_t)m * e.ld_out;
+      int kind = 2, head = 0, w = 0;
+      if (e.which == 0) qkv_classify(e, f0, kind, head, w);
+      if (e.which == 0 && kind == 2) {
+        uint4 o0, o1;
+        uint32_t* p0 = reinterpret_cast<uint32_t*>(&o0);
+        uint32_t* p1 = reinterpret_cast<uint32_t*>(&o1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          p0[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+          p1[j] = pack_bf16x2(v[8 + 2 * j], v[9 + 2 * j]);
+        }
+        reinterpret_cast<uint4*>(row + f0)[0] = o0;
+        reinterpret_cast<uint4*>(row + f0)[1] = o1;
+      } else {
+        // 8 pairs: first halves go to one run of 8 columns, second halves to another
+        uint4 lo, hi;
+        uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+        uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          pl[j] = pack_bf16x2(v[4 * j], v[4 * j + 2]);
+          ph[j] = pack_bf16x2(v[4 * j + 1], v[4 * j + 3]);
+        }
+        int c_lo, c_hi;
+        if (e.which == 1) { c_lo = f0 >> 1; c_hi = e.inter_per_rank + (f0 >> 1); }
+        else { c_lo = f0 - w + (w >> 1); c_hi = c_lo + e.head_dim / 2; }
+        *reinterpret_cast<uint4*>(row + c_lo) = lo;
+        *reinterpret_cast<uint4*>(row + c_hi) = hi;
+      }
+    } else if constexpr (EPI == EPI_LOGITS) {
+      uint16_t* row = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int f = f0 + j;
+        const int64_t col = (int64_t)g * e.vocab_per_rank + f;
+        if (f < e.vocab_per_rank && col < e.vocab) row[col] = f_to_bf16(v[j]);
+      }
+    } else if constexpr (EPI == EPI_SILU) {
+      uint16_t* row = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out +
+                      (int64_t)g * e.inter_per_rank + (f0 >> 1);
+      uint4 o;
+      uint32_t* p = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float g0 = v[4 * j], u0 = v[4 * j + 1], g1 = v[4 * j + 2], u1 = v[4 * j + 3];
+        p[j] = pack_bf16x2(g0 / (1.f + expf(-g0)) * u0, g1 / (1.f + expf(-g1)) * u1);
+      }
+      *reinterpret_cast<uint4*>(row) = o;
+    } else if constexpr (EPI == EPI_QKV) {
+      int kind, head, w;
+      qkv_classify(e, f0, kind, head, w);
+      const int d = e.head_dim, half = d / 2;
+      const int pos = e.positions[m];
+      if (pos < 0 || pos >= e.l_max) return;  // never index the cache or table out of range
+      float outv[16];
+      if (kind == 2) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) outv[j] = v[j];
+      } else {
+        const float2* cs = e.rope + (int64_t)pos * half + (w >> 1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 c = cs[j];
+          const float x1 = v[2 * j], x2 = v[2 * j + 1];
+          outv[j] = x1 * c.x - x2 * c.y;       // feature jp
+          outv[8 + j] = x2 * c.x + x1 * c.y;   // feature jp + d/2
+        }
+      }
+      uint4 lo, hi;
+      uint32_t* pl = reinterpret_cast<uint32_t*>(&lo);
+      uint32_t* ph = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pl[j] = pack_bf16x2(outv[2 * j], outv[2 * j + 1]);
+        ph[j] = pack_bf16x2(outv[8 + 2 * j], outv[9 + 2 * j]);
+      }
+      // destination runs: V rows are in natural order; Q/K pairs split in two runs
+      const int c_lo = kind == 2 ? w : (w >> 1);
+      const int c_hi = kind == 2 ? w + 8 : (w >> 1) + half;
+      if (kind == 0) {
+        uint16_t* dst = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out +
+                        (int64_t)(g * e.q_heads_per_rank + head) * d;
+        *reinterpret_cast<uint4*>(dst + c_lo) = lo;
+        *reinterpret_cast<uint4*>(dst + c_hi) = hi;
+      } else if ((g % e.kv_replicas) == 0) {
+        const int seq = e.token_seq[m];
+        uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
+        uint16_t* dst = cache + (int64_t)(g / e.kv_replicas) * e.kv_copy_stride +
+                        (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d;
+        *reinterpret_cast<uint4*>(dst + c_lo) = lo;
+        *reinterpret_cast<uint4*>(dst + c_hi) = hi;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+template <bool SWAP, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int BN = a.BN, S = a.stages;
+  const int b_tile_bytes = BN * 128;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * b_tile_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    mbar_init(drain, 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&a.tmA); tma_prefetch_desc(&a.tmB); }
+  if (warp == 1) { tmem_alloc(tmem_slot, a.tmem_cols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int G = a.grid, c = blockIdx.x;
+  const int64_t T = a.total_iters;
+  const int K = a.k_slices * a.k_iters_slice;  // K steps per tile
+  const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int64_t it = beg; it < end && ok;) {
+        const int64_t tile = it / K;
+        const int64_t seg_end = min(end, (tile + 1) * K);
+        const int ia = static_cast<int>(tile % a.a_tiles);
+        const int64_t rest = tile / a.a_tiles;
+        const int ib = static_cast<int>(rest % a.b_tiles);
+        const int g = static_cast<int>(rest / a.b_tiles);
+        for (int k = static_cast<int>(it - tile * K); k < static_cast<int>(seg_end - tile * K); ++k) {
+          const uint32_t s = n % S, ph = (n / S) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, a.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kATileBytes + b_tile_bytes);
+          const int ks = k / a.k_iters_slice, kk = k - ks * a.k_iters_slice;
+          const int sa = slice_of(a.a_slice_mode, g, ks), sb = slice_of(a.b_slice_mode, g, ks);
+          if (a.a_slice_mid)
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, sa, ia * 128, polA);
+          else
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, ia * 128, sa, polA);
+          if (a.b_slice_mid)
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, sb, ib * BN, polB);
+          else
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, ib * BN, sb, polB);
+          ++n;
+        }
+        it = seg_end;
+      }
+      // never leave with bulk copies still landing in shared memory
+      for (uint32_t i = (n > (uint32_t)S ? n - S : 0); i < n; ++i)
+        mbar_wait(&full[i % S], (i / S) & 1, a.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      uint32_t n = 0, seg = 0;
+      bool ok = true;
+      for (int64_t it = beg; it < end && ok;) {
+        const int64_t tile = it / K;
+        const int64_t seg_end = min(end, (tile + 1) * K);
+        const uint32_t buf = seg & 1, use = seg >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, a.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + buf * BN;
+        const int k0 = static_cast<int>(it - tile * K), k1 = static_cast<int>(seg_end - tile * K);
+        for (int k = k0; k < k1; ++k) {
+          const uint32_t s = n % S, ph = (n / S) & 1;
+          if (!mbar_wait(&full[s], ph, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = smem_desc_sw128(sA + s * kATileBytes);
+          const uint64_t db = smem_desc_sw128(sB + s * b_tile_bytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (k > k0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+          ++n;
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[buf]);
+        ++seg;
+        it = seg_end;
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.status);
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    uint32_t seg = 0;
+    for (int64_t it = beg; it < end;) {
+      const int64_t tile = it / K;
+      const int64_t seg_end = min(end, (tile + 1) * K);
+      const int ia = static_cast<int>(tile % a.a_tiles);
+      const int64_t rest = tile / a.a_tiles;
+      const int ib = static_cast<int>(rest % a.b_tiles);
+      const int g = static_cast<int>(rest / a.b_tiles);
+      const uint32_t buf = seg & 1, use = seg >> 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&acc_full[buf], use & 1, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (bar_sync_or(1, 128, !ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
+      const int arow = ia * 128 + row;
+      const int brow = ib * BN;
+      const int c_first = owner_of(tile * K, T, G);
+      const int c_last = owner_of((tile + 1) * K - 1, T, G);
+      const int nseg = c_last - c_first + 1;
+      if (nseg == 1) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
+          epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      } else {
+        // my piece of the tile -> workspace slot 0 (tile where my range starts) or 1
+        const int my_slot = (beg / K == tile) ? 0 : 1;
+        float* mine = a.partials + ((int64_t)(c * 2 + my_slot) * BN) * 128;
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mine[(c0 + j) * 128 + row] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        __threadfence();
+        bar_sync(1, 128);
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(&a.tickets[tile], 1);
+          *last_flag = (old == nseg - 1) ? 1 : 0;
+        }
+        bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int sgi = 0; sgi < nseg; ++sgi) {
+              const int cc = c_first + sgi;
+              const int slot = (range_begin(cc, T, G) / K == tile) ? 0 : 1;
+              const float* src = a.partials + ((int64_t)(cc * 2 + slot) * BN) * 128;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(&src[(c0 + j) * 128 + row]);
+            }
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v);
+          }
+          if (threadIdx.x == 64) a.tickets[tile] = 0;
+        }
+        bar_sync(1, 128);
+      }
+      ++seg;
+      it = seg_end;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+}  // namespace tpk

@@ -1,0 +1,122 @@
+// Declarations shared by the translation units of the library: kernel
+// argument blocks and host-side launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tpk {
+
+enum Epi : int {
+  EPI_PLAIN = 0,    // column-parallel output, standard per-rank order
+  EPI_QKV = 1,      // RoPE on q,k; q -> q buffer, k,v -> rank cache
+  EPI_SILU = 2,     // SiLU(gate) * up
+  EPI_RESID = 3,    // fused row-parallel: y = residual + sum of rank partials
+  EPI_PARTIAL = 4,  // unfused row-parallel: fp32 partial of each rank
+  EPI_LOGITS = 5,   // LM head: logits placed in the rank's vocab slot
+};
+
+struct EpiArgs {
+  int M;                    // tokens
+  void* out;                // bf16 (or fp32 for EPI_PARTIAL)
+  int64_t ld_out;           // row stride of out (elements)
+  int64_t out_group_stride; // elements between ranks' outputs (PLAIN, PARTIAL)
+  const uint16_t* residual; // EPI_RESID, may be null
+  int64_t ld_res;
+  int which;                // EPI_PLAIN: 0 = qkv layout, 1 = gate_up layout
+  int head_dim;
+  int q_heads_per_rank;
+  int kv_heads_per_rank;
+  int kv_replicas;
+  int inter_per_rank;
+  // EPI_QKV
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int64_t kv_copy_stride;   // elements per rank copy
+  int n_seqs;
+  int l_max;
+  const int32_t* positions;
+  const int32_t* token_seq;
+  const float2* rope;       // [max_positions][head_dim/2] (cos, sin)
+  // EPI_LOGITS
+  int vocab;
+  int vocab_per_rank;
+};
+
+struct GemmArgs {
+  CUtensorMap tmA;          // (K, rows, slices), box (64, 128, 1)
+  CUtensorMap tmB;          // (K, rows, slices), box (64, BN, 1)
+  int BN;                   // N tile: multiple of 16, <= 256
+  int stages;
+  int tmem_cols;            // power of two >= 2*BN
+  int n_groups;             // output groups (ranks) on the tile axis
+  int a_tiles, b_tiles;     // tiles per group along A rows / B rows
+  int k_slices;             // rank slices folded into K (fused row-parallel)
+  int k_iters_slice;        // 64-wide K steps per slice
+  int a_slice_mode;         // 0: slice 0; 1: slice = group; 2: slice = K slice
+  int b_slice_mode;
+  int a_rows_valid;         // A rows per group that exist
+  int b_rows_valid;         // B rows per group that exist
+  int a_policy, b_policy;   // L2 policy: 0 normal, 1 evict_first, 2 evict_last
+  int a_slice_mid, b_slice_mid;  // 1: tensor map dims are (K, slice, rows)
+  int grid;                 // G
+  int64_t total_iters;      // n_tiles * k_slices * k_iters_slice
+  float* partials;          // [G][2][BN][128]
+  int* tickets;             // [n_tiles], zero on entry and exit
+  int* status;              // device status word
+  EpiArgs e;
+};
+
+struct AttnArgs {
+  CUtensorMap tmK;            // (d, l_max, copies*n_seqs*kv_r), box (64, 64, 1)
+  CUtensorMap tmV;
+  const uint16_t* q;          // [M, n_heads*d]
+  int64_t ld_q;
+  uint16_t* o;                // [M, n_heads*d]
+  int64_t ld_o;
+  const int32_t* positions;
+  const int32_t* seq_start;   // prefill
+  int n_seqs, n_heads, n_kv, head_dim, kv_r, group;
+  int l_max;                  // cache capacity per sequence
+  float scale_log2;           // log2(e) / sqrt(d)
+  // decode: even split of (sequence, KV head, key tile) units over the grid
+  int tiles_per_bg;
+  int64_t total_units;
+  int grid;
+  float* partials;            // [grid][2][16][d+2]
+  int* tickets;               // [n_seqs*n_kv]
+  int* status;
+};
+
+// gemm.cu / gemm_epi*.cu
+cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st);
+#define TPK_DECLARE_EPI(E) \
+  cudaError_t launch_gemm_epi##E(bool swap, const GemmArgs& a, size_t smem, cudaStream_t st);
+TPK_DECLARE_EPI(0)
+TPK_DECLARE_EPI(1)
+TPK_DECLARE_EPI(2)
+TPK_DECLARE_EPI(3)
+TPK_DECLARE_EPI(4)
+TPK_DECLARE_EPI(5)
+
+// attention.cu
+cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_prefill(const AttnArgs& a, int n_qb, cudaStream_t st);
+size_t attn_decode_partial_floats(int head_dim);
+size_t attn_decode_smem_bytes(int head_dim);
+
+// small.cu
+cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,
+                         const int32_t* ids, int M, int H, uint16_t* h, int* status,
+                         cudaStream_t st);
+cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
+                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st);
+cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int t, int M, int H,
+                                const uint16_t* residual, uint16_t* y, cudaStream_t st);
+cudaError_t launch_rope_table(float2* table, int max_pos, int head_dim, double theta,
+                              cudaStream_t st);
+cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
+                             const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st);
+
+}  // namespace tpk

@@ -1,0 +1,212 @@
+// Memory-bound kernels of the layer: vocab-parallel embedding, replicated
+// RMSNorm, the separate rank-ordered reduction of the unfused row-parallel
+// variant, the RoPE table and the shard builder's row copies.  All move
+// 16-byte vectors with consecutive threads on consecutive addresses.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpk {
+
+// ---------------------------------------------------------------------------
+// Vocab-parallel embedding ("第 9 章 多进程与张量并行", §3.2 Vocab Parallel;
+// "张量、流水线与数据并行", 线性层怎么切: 词嵌入).  Rank r holds vocab rows
+// [r Vp/t, (r+1) Vp/t); a token contributes its row on the owner rank and -0.0
+// on every other rank, and the all-reduce sums the t contributions in rank
+// order.  Because x + (-0.0) == x for every x, that sum is the owner's row bit
+// for bit, so the kernel copies the owner's row: the masked lookups of the
+// other ranks and the reduction are exact no-ops it does not need to execute.
+// One warp per token; the t shards are stored back to back, so rank r's local
+// row l sits at padded row r*Vp/t + l.
+// ---------------------------------------------------------------------------
+__global__ void embed_kernel(const uint16_t* __restrict__ table, int vocab, int vocab_per_rank,
+                             int t, const int32_t* __restrict__ ids, int M, int H,
+                             uint16_t* __restrict__ h, int* status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const int id = ids[warp];
+  uint4* dst = reinterpret_cast<uint4*>(h + (int64_t)warp * H);
+  const int nvec = H / 8;
+  if (id < 0 || id >= vocab) {
+    if (lane == 0) record_status(status, kStatusTokenRange);
+    for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int owner = id / vocab_per_rank;          // the one rank whose lookup hits
+  const int local = id - owner * vocab_per_rank;  // row inside that rank's shard
+  const uint4* src = reinterpret_cast<const uint4*>(
+      table + ((int64_t)owner * vocab_per_rank + local) * H);
+  for (int i = lane; i < nvec; i += 32) dst[i] = __ldg(&src[i]);
+}
+
+cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,
+                         const int32_t* ids, int M, int H, uint16_t* h, int* status,
+                         cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const int blocks = (M + warps_per_block - 1) / warps_per_block;
+  embed_kernel<<<blocks, warps_per_block * 32, 0, st>>>(table, vocab, vocab_per_rank, t, ids, M,
+                                                         H, h, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm, replicated on every rank ("第 9 章", §3.2: small layers such as
+// RMSNorm are copied whole to each rank): one copy serves all emulated ranks.
+// y = x / sqrt(mean(x^2) + eps) * w in fp32; one CTA per row.  With `rows`,
+// row i of y normalises row rows[i] of x (the sampled rows before the head).
+// ---------------------------------------------------------------------------
+constexpr int kNormThreads = 256;
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
+    const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ rows,
+    const uint16_t* __restrict__ w, int H, float eps, uint16_t* __restrict__ y, int64_t ldy) {
+  __shared__ float red[kNormThreads / 32];
+  const int i = blockIdx.x;
+  const int src_row = rows ? rows[i] : i;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)src_row * ldx);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  uint4* yr = reinterpret_cast<uint4*>(y + (int64_t)i * ldy);
+  const int nvec = H / 8;
+  float ss = 0.f;
+  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
+    const uint4 p = xr[v];
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&p);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float f = bf16_to_f(e[j]);
+      ss = fmaf(f, f, ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int k = 0; k < kNormThreads / 32; ++k) tot += red[k];
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
+    const uint4 p = xr[v], q = wr[v];
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&p);
+    const uint16_t* g = reinterpret_cast<const uint16_t*>(&q);
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      op[j] = pack_bf16x2(bf16_to_f(e[2 * j]) * inv * bf16_to_f(g[2 * j]),
+                          bf16_to_f(e[2 * j + 1]) * inv * bf16_to_f(g[2 * j + 1]));
+    yr[v] = o;
+  }
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
+                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(x, ldx, rows, w, H, eps, y, ldy);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Unfused row-parallel reduction: y = (P_0 + P_1 + ... + P_{t-1}) + residual,
+// summed in fp32 in rank order and rounded once to bf16 ("第 9 章", §3.1: the
+// all-reduce of a row-parallel layer is a sum).  P_r: [M, H] fp32 partials.
+// ---------------------------------------------------------------------------
+__global__ void reduce_ranks_kernel(const float4* __restrict__ P, int64_t rank_stride4, int t,
+                                    int64_t n4, int H4, const uint2* __restrict__ residual,
+                                    uint2* __restrict__ y) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 acc = P[i];
+    for (int r = 1; r < t; ++r) {
+      const float4 p = P[r * rank_stride4 + i];
+      acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    if (residual) {
+      const uint2 rv = residual[i];
+      acc.x += __uint_as_float(rv.x << 16);
+      acc.y += __uint_as_float(rv.x & 0xFFFF0000u);
+      acc.z += __uint_as_float(rv.y << 16);
+      acc.w += __uint_as_float(rv.y & 0xFFFF0000u);
+    }
+    y[i] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+}
+
+cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int t, int M, int H,
+                                const uint16_t* residual, uint16_t* y, cudaStream_t st) {
+  const int64_t n4 = (int64_t)M * H / 4;
+  if (n4 == 0) return cudaSuccess;
+  int blocks = (int)((n4 + 255) / 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  reduce_ranks_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(partials),
+                                              rank_stride / 4, t, n4, H / 4,
+                                              reinterpret_cast<const uint2*>(residual),
+                                              reinterpret_cast<uint2*>(y));
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RoPE table: (cos, sin) of p * theta^(-2j/d), evaluated in double, stored as
+// float, for p < max_pos and j < d/2 (rotate-half pairing of j and j + d/2).
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* table, int max_pos, int half, int head_dim,
+                                  double theta) {
+  const int64_t n = (int64_t)max_pos * half;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / half), j = (int)(i % half);
+    const double inv_freq = pow(theta, -(2.0 * j) / head_dim);
+    double s, c;
+    sincos((double)p * inv_freq, &s, &c);
+    table[i] = make_float2((float)c, (float)s);
+  }
+}
+
+cudaError_t launch_rope_table(float2* table, int max_pos, int head_dim, double theta,
+                              cudaStream_t st) {
+  const int half = head_dim / 2;
+  const int64_t n = (int64_t)max_pos * half;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  rope_table_kernel<<<blocks, 256, 0, st>>>(table, max_pos, half, head_dim, theta);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Shard builder: dst row i <- src row row_map[i] (n_cols elements), or zeros
+// when row_map[i] < 0.  Used once at load time.
+// ---------------------------------------------------------------------------
+__global__ void copy_rows_kernel(uint16_t* __restrict__ dst, int64_t dst_ld,
+                                 const uint16_t* __restrict__ src, int64_t src_ld,
+                                 const int32_t* __restrict__ row_map, int n_cols, bool vec) {
+  const int i = blockIdx.x;
+  const int sr = row_map[i];
+  uint16_t* d = dst + (int64_t)i * dst_ld;
+  if (vec) {
+    uint4* d4 = reinterpret_cast<uint4*>(d);
+    const uint4* s4 = sr >= 0 ? reinterpret_cast<const uint4*>(src + (int64_t)sr * src_ld) : nullptr;
+    for (int c = threadIdx.x; c < n_cols / 8; c += blockDim.x)
+      d4[c] = s4 ? s4[c] : make_uint4(0, 0, 0, 0);
+  } else {
+    const uint16_t* s = sr >= 0 ? src + (int64_t)sr * src_ld : nullptr;
+    for (int c = threadIdx.x; c < n_cols; c += blockDim.x) d[c] = s ? s[c] : 0;
+  }
+}
+
+cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
+                             const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const bool vec = (n_cols % 8 == 0) && (dst_ld % 8 == 0) && (src_ld % 8 == 0) &&
+                   (reinterpret_cast<uintptr_t>(dst) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(src) % 16 == 0);
+  copy_rows_kernel<<<n_rows, 256, 0, st>>>(dst, dst_ld, src, src_ld, row_map, n_cols, vec);
+  return cudaGetLastError();
+}
+
+}  // namespace tpk

@@ -1,0 +1,822 @@
+// Host side of the C ABI declared in include/tp.h: configuration rules, shard
+// construction, TMA descriptors, work planning and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "tp.h"
+
+using namespace tpk;
+
+struct ShardedLinear {
+  uint16_t* data = nullptr;  // [t][rows][cols]
+  int rows = 0, cols = 0;    // per rank
+  CUtensorMap tm_a;          // box (64, 128, 1): weight on the MMA M side (decode)
+  CUtensorMap tm_b;          // box (64, 256, 1): weight on the MMA N side (prefill)
+};
+
+struct LayerShards {
+  ShardedLinear qkv, gate_up, o, down;
+  uint16_t* attn_norm = nullptr;
+  uint16_t* mlp_norm = nullptr;
+};
+
+struct tp_model {
+  tp_config_t cfg;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<LayerShards> layers;
+  uint16_t* embed = nullptr;  // [Vp][H] = t shards of [Vp/t][H]
+  ShardedLinear lm;
+  uint16_t* final_norm = nullptr;
+  float2* rope = nullptr;
+  int* status = nullptr;
+  std::vector<void*> allocs;
+  mutable tp_stats_t stats;
+};
+
+namespace {
+
+constexpr int kPrefillBN = 256;
+constexpr int kSwapMaxTokens = 64;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map (inner K, rows, slices) with a (64, box_rows, 1) box and
+// 128-byte swizzle; reads outside the extents return zeros.
+// When the slices sit closer together than the rows (rank shards side by side
+// in one [rows, t*K] buffer), the dimensions are ordered (K, slice, rows) so
+// the strides increase; *slice_mid reports which order was used.
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t slices,
+               uint64_t row_stride_bytes, uint64_t slice_stride_bytes, uint32_t box_rows,
+               int* slice_mid = nullptr) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const bool mid = slices > 1 && slice_stride_bytes < row_stride_bytes;
+  if (slice_mid) *slice_mid = mid ? 1 : 0;
+  if (mid && !slice_mid) return false;
+  cuuint64_t dims[3] = {inner, rows, slices};
+  cuuint64_t strides[2] = {row_stride_bytes, slice_stride_bytes};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  if (mid) {
+    dims[1] = slices; dims[2] = rows;
+    strides[0] = slice_stride_bytes; strides[1] = row_stride_bytes;
+    box[1] = 1; box[2] = box_rows;
+  }
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+tp_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TP_OK;
+  if (e == cudaErrorMemoryAllocation) return TP_ERR_OOM;
+  return TP_ERR_CUDA;
+}
+
+#define TP_CHECK_CUDA(expr)                         \
+  do {                                              \
+    cudaError_t _e = (expr);                        \
+    if (_e != cudaSuccess) return cuda_status(_e);  \
+  } while (0)
+
+template <class T>
+tp_status dev_alloc(tp_model* m, T** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+  if (e != cudaSuccess) return cuda_status(e);
+  m->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  return TP_OK;
+}
+
+// ---------------------------------------------------------------- planning
+struct GemmPlan {
+  bool swap;
+  int BN, stages, tmem_cols;
+  size_t smem;
+};
+
+GemmPlan plan_gemm(int M) {
+  GemmPlan p;
+  p.swap = M <= kSwapMaxTokens;
+  p.BN = p.swap ? std::max(16, cdiv(M, 16) * 16) : kPrefillBN;
+  const int stage = 128 * 128 + p.BN * 128;
+  const int budget = 200 * 1024;
+  p.stages = std::min(8, budget / stage);
+  int cols = 32;
+  while (cols < 2 * p.BN) cols *= 2;
+  p.tmem_cols = cols;
+  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16;
+  return p;
+}
+
+// Workspace regions (all offsets 256-byte aligned).
+struct WsLayout {
+  size_t gemm_tickets, attn_tickets, gemm_partials, attn_partials, u, q, o, act, hs, rank_partials,
+      total;
+};
+
+size_t max_gemm_tiles(const tp_config_t& c, int M) {
+  // upper bound over every GEMM of the model for M tokens
+  const int H = c.hidden, d = c.head_dim, t = c.t;
+  const int nqkv = (c.q_heads_per_rank + 2 * c.kv_heads_per_rank) * d;
+  const int rows[4] = {nqkv, 2 * c.inter_per_rank, H, std::max(c.vocab_per_rank, 1)};
+  size_t best = 0;
+  for (int r : rows) {
+    // decode orientation
+    best = std::max(best, (size_t)t * cdiv(r, 128));
+    // prefill orientation
+    best = std::max(best, (size_t)t * cdiv(M, 128) * cdiv(r, kPrefillBN));
+  }
+  return best;
+}
+
+WsLayout ws_layout(const tp_model* m, int M) {
+  const tp_config_t& c = m->cfg;
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const int G = m->num_sms;
+  L.gemm_tickets = take(max_gemm_tiles(c, M) * sizeof(int));
+  L.attn_tickets = take((size_t)std::max(M, 1) * c.n_kv_heads * sizeof(int));
+  L.gemm_partials = take((size_t)G * 2 * kPrefillBN * 128 * sizeof(float));
+  L.attn_partials = take((size_t)G * 2 * attn_decode_partial_floats(c.head_dim) * sizeof(float));
+  L.u = take((size_t)M * c.hidden * 2);
+  L.q = take((size_t)M * c.n_heads * c.head_dim * 2);
+  L.o = take((size_t)M * c.n_heads * c.head_dim * 2);
+  L.act = take((size_t)M * c.intermediate * 2);
+  L.hs = take((size_t)M * c.hidden * 2);
+  L.rank_partials = take((size_t)c.t * M * c.hidden * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+bool ws_ok(const tp_model* m, int M, const void* ws, size_t bytes) {
+  return ws != nullptr && aligned16(ws) && bytes >= ws_layout(m, M).total;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+EpiArgs base_epi(const tp_model* m, int M) {
+  EpiArgs e;
+  memset(&e, 0, sizeof(e));
+  e.M = M;
+  e.head_dim = m->cfg.head_dim;
+  e.q_heads_per_rank = m->cfg.q_heads_per_rank;
+  e.kv_heads_per_rank = m->cfg.kv_heads_per_rank;
+  e.kv_replicas = m->cfg.kv_replicas;
+  e.inter_per_rank = m->cfg.inter_per_rank;
+  e.vocab = m->cfg.vocab;
+  e.vocab_per_rank = m->cfg.vocab_per_rank;
+  return e;
+}
+
+// Column-parallel family (qkv, gate_up, LM head): each rank r produces its own
+// [M, rows] output from the replicated x [M, K].
+tp_status run_column(const tp_model* m, const ShardedLinear& W, const uint16_t* x, int64_t ldx,
+                     int M, int epi, const EpiArgs& e, void* ws, const WsLayout& L,
+                     cudaStream_t st) {
+  if (M == 0) return TP_OK;
+  const tp_config_t& c = m->cfg;
+  const int K = W.cols;
+  GemmPlan p = plan_gemm(M);
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  bool ok;
+  if (p.swap) {
+    a.tmA = W.tm_a;
+    ok = make_tmap(&a.tmB, x, K, M, 1, ldx * 2, (uint64_t)ldx * 2 * M, p.BN);
+    a.a_tiles = cdiv(W.rows, 128);
+    a.b_tiles = 1;
+    a.a_slice_mode = 1;
+    a.b_slice_mode = 0;
+    a.a_rows_valid = W.rows;
+    a.b_rows_valid = M;
+    a.a_policy = 1;
+    a.b_policy = 2;
+  } else {
+    ok = make_tmap(&a.tmA, x, K, M, 1, ldx * 2, (uint64_t)ldx * 2 * M, 128);
+    a.tmB = W.tm_b;
+    a.a_tiles = cdiv(M, 128);
+    a.b_tiles = cdiv(W.rows, p.BN);
+    a.a_slice_mode = 0;
+    a.b_slice_mode = 1;
+    a.a_rows_valid = M;
+    a.b_rows_valid = W.rows;
+  }
+  if (!ok) return TP_ERR_CUDA;
+  a.BN = p.BN;
+  a.stages = p.stages;
+  a.tmem_cols = p.tmem_cols;
+  a.n_groups = c.t;
+  a.k_slices = 1;
+  a.k_iters_slice = cdiv(K, 64);
+  a.total_iters = (int64_t)a.n_groups * a.a_tiles * a.b_tiles * a.k_iters_slice;
+  a.grid = (int)std::min<int64_t>(m->num_sms, a.total_iters);
+  a.partials = at<float>(ws, L.gemm_partials);
+  a.tickets = at<int>(ws, L.gemm_tickets);
+  a.status = m->status;
+  a.e = e;
+  m->stats.kernel_launches++;
+  return cuda_status(launch_gemm(p.swap, epi, a, p.smem, st));
+}
+
+// Row-parallel family (o_proj, down_proj): rank r holds W_r [H, K_r] and reads
+// x_r [M, K_r]; fused = sum over ranks inside the GEMM (epilogue EPI_RESID),
+// otherwise per-rank fp32 partials then the ordered reduction kernel.
+tp_status run_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
+                  int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
+                  uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st) {
+  if (M == 0) return TP_OK;
+  const tp_config_t& c = m->cfg;
+  const int Kr = W.cols, H = W.rows, t = c.t;
+  GemmPlan p = plan_gemm(M);
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t xs_bytes = (uint64_t)x_rank_stride * 2;
+  bool ok;
+  if (p.swap) {
+    a.tmA = W.tm_a;
+    ok = make_tmap(&a.tmB, x, Kr, M, t, ldx * 2, xs_bytes, p.BN, &a.b_slice_mid);
+    a.a_tiles = cdiv(H, 128);
+    a.b_tiles = 1;
+    a.a_rows_valid = H;
+    a.b_rows_valid = M;
+    a.a_policy = 1;
+    a.b_policy = 2;
+  } else {
+    ok = make_tmap(&a.tmA, x, Kr, M, t, ldx * 2, xs_bytes, 128, &a.a_slice_mid);
+    a.tmB = W.tm_b;
+    a.a_tiles = cdiv(M, 128);
+    a.b_tiles = cdiv(H, p.BN);
+    a.a_rows_valid = M;
+    a.b_rows_valid = H;
+  }
+  if (!ok) return TP_ERR_CUDA;
+  a.BN = p.BN;
+  a.stages = p.stages;
+  a.tmem_cols = p.tmem_cols;
+  a.k_iters_slice = cdiv(Kr, 64);
+  a.partials = at<float>(ws, L.gemm_partials);
+  a.tickets = at<int>(ws, L.gemm_tickets);
+  a.status = m->status;
+  a.e = base_epi(m, M);
+  int epi;
+  float* rp = at<float>(ws, L.rank_partials);
+  if (fused) {
+    a.n_groups = 1;
+    a.k_slices = t;  // ranks folded into K, in rank order
+    a.a_slice_mode = 2;
+    a.b_slice_mode = 2;
+    a.e.out = y;
+    a.e.ld_out = H;
+    a.e.residual = residual;
+    a.e.ld_res = H;
+    epi = EPI_RESID;
+  } else {
+    a.n_groups = t;
+    a.k_slices = 1;
+    a.a_slice_mode = 1;
+    a.b_slice_mode = 1;
+    a.e.out = rp;
+    a.e.ld_out = H;
+    a.e.out_group_stride = (int64_t)M * H;
+    epi = EPI_PARTIAL;
+  }
+  a.total_iters = (int64_t)a.n_groups * a.a_tiles * a.b_tiles * a.k_slices * a.k_iters_slice;
+  a.grid = (int)std::min<int64_t>(m->num_sms, a.total_iters);
+  m->stats.kernel_launches++;
+  TP_CHECK_CUDA(launch_gemm(p.swap, epi, a, p.smem, st));
+  if (!fused) {
+    m->stats.kernel_launches++;
+    TP_CHECK_CUDA(launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, residual, y, st));
+  }
+  m->stats.allreduces++;
+  m->stats.allreduce_payload_bytes += (int64_t)M * H * 2;
+  return TP_OK;
+}
+
+bool valid_layer(const tp_model* m, int layer) {
+  return m && layer >= 0 && layer < (int)m->layers.size();
+}
+
+// Builds one sharded weight: t ranks of [rows][cols]; rank r's rows come from
+// the calls the caller makes through `fill` (copy_rows launches).
+tp_status alloc_linear(tp_model* m, ShardedLinear* L, int rows, int cols) {
+  L->rows = rows;
+  L->cols = cols;
+  tp_status s = dev_alloc(m, &L->data, (size_t)m->cfg.t * rows * cols * 2);
+  if (s != TP_OK) return s;
+  const uint64_t rs = (uint64_t)cols * 2, ss = (uint64_t)rows * cols * 2;
+  if (!make_tmap(&L->tm_a, L->data, cols, rows, m->cfg.t, rs, ss, 128)) return TP_ERR_CUDA;
+  if (!make_tmap(&L->tm_b, L->data, cols, rows, m->cfg.t, rs, ss, kPrefillBN)) return TP_ERR_CUDA;
+  return TP_OK;
+}
+
+struct MapUploader {
+  std::vector<int32_t*> bufs;
+  ~MapUploader() {
+    for (auto* b : bufs) cudaFree(b);
+  }
+  tp_status upload(const std::vector<int32_t>& v, int32_t** out, cudaStream_t st) {
+    int32_t* d = nullptr;
+    cudaError_t e = cudaMalloc(&d, std::max<size_t>(v.size(), 1) * 4);
+    if (e != cudaSuccess) return cuda_status(e);
+    bufs.push_back(d);
+    e = cudaMemcpyAsync(d, v.data(), v.size() * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    *out = d;
+    return TP_OK;
+  }
+};
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+namespace tpk {
+cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st) {
+  switch (epi) {
+    case 0: return launch_gemm_epi0(swap, a, smem, st);
+    case 1: return launch_gemm_epi1(swap, a, smem, st);
+    case 2: return launch_gemm_epi2(swap, a, smem, st);
+    case 3: return launch_gemm_epi3(swap, a, smem, st);
+    case 4: return launch_gemm_epi4(swap, a, smem, st);
+    case 5: return launch_gemm_epi5(swap, a, smem, st);
+  }
+  return cudaErrorInvalidValue;
+}
+}  // namespace tpk
+
+extern "C" {
+
+const char* tp_strerror(tp_status s) {
+  switch (s) {
+    case TP_OK: return "ok";
+    case TP_ERR_ARG: return "invalid argument";
+    case TP_ERR_DIVISIBILITY: return "dimension not divisible by the number of ranks";
+    case TP_ERR_KV_REPLICA: return "KV heads can be neither split evenly nor replicated evenly";
+    case TP_ERR_TOKEN_RANGE: return "token id outside [0, vocab)";
+    case TP_ERR_OOM: return "device allocation failed";
+    case TP_ERR_CUDA: return "CUDA runtime error";
+    case TP_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case TP_ERR_UNSUPPORTED: return "shape outside the kernels' envelope";
+    case TP_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+tp_status tp_config(tp_config_t* c) {
+  if (!c) return TP_ERR_ARG;
+  if (c->t < 1 || c->hidden < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+      c->intermediate < 1 || c->vocab < 0 || c->n_layers < 0 || c->max_positions < 1 ||
+      !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
+    return TP_ERR_ARG;
+  const int t = c->t;
+  if (c->n_heads % c->n_kv_heads) return TP_ERR_DIVISIBILITY;
+  if (c->n_heads % t) return TP_ERR_DIVISIBILITY;
+  if (c->intermediate % t) return TP_ERR_DIVISIBILITY;
+  int kv_r, reps;
+  if (c->n_kv_heads >= t) {
+    if (c->n_kv_heads % t) return TP_ERR_KV_REPLICA;
+    kv_r = c->n_kv_heads / t;
+    reps = 1;
+  } else {
+    if (t % c->n_kv_heads) return TP_ERR_KV_REPLICA;
+    kv_r = 1;
+    reps = t / c->n_kv_heads;
+  }
+  const int vp = (c->vocab + t - 1) / t * t;
+  c->vocab_padded = vp;
+  c->vocab_per_rank = vp / t;
+  c->q_heads_per_rank = c->n_heads / t;
+  c->kv_heads_per_rank = kv_r;
+  c->kv_replicas = reps;
+  c->kv_copies = std::min(t, c->n_kv_heads);
+  c->inter_per_rank = c->intermediate / t;
+  // kernel envelope
+  if (t > 8) return TP_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return TP_ERR_UNSUPPORTED;
+  if (c->hidden % 64 || (c->q_heads_per_rank * c->head_dim) % 64 || c->inter_per_rank % 64)
+    return TP_ERR_UNSUPPORTED;
+  if (c->n_heads / c->n_kv_heads > 16) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+tp_status tp_get_config(const tp_model* m, tp_config_t* out) {
+  if (!m || !out) return TP_ERR_ARG;
+  *out = m->cfg;
+  return TP_OK;
+}
+
+void tp_free(tp_model* m) {
+  if (!m) return;
+  for (void* p : m->allocs) cudaFree(p);
+  delete m;
+}
+
+tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void* stream,
+                         tp_model** out) {
+  if (!cfg_in || !w || !out) return TP_ERR_ARG;
+  *out = nullptr;
+  tp_config_t cfg = *cfg_in;
+  tp_status s = tp_config(&cfg);
+  if (s != TP_OK) return s;
+  if (cfg.n_layers > 0 && !w->layers) return TP_ERR_ARG;
+  for (int l = 0; l < cfg.n_layers; ++l) {
+    const tp_layer_weights_t& L = w->layers[l];
+    if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.mlp_norm || !L.wg || !L.wu || !L.wd)
+      return TP_ERR_ARG;
+  }
+  if ((w->embed || w->lm_head || w->final_norm) && cfg.vocab < 1) return TP_ERR_ARG;
+  if (!get_encoder()) return TP_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  tp_model* m = new tp_model();
+  m->cfg = cfg;
+  memset(&m->stats, 0, sizeof(m->stats));
+  auto fail = [&](tp_status e) {
+    cudaStreamSynchronize(st);
+    tp_free(m);
+    return e;
+  };
+  if (cudaGetDevice(&m->device) != cudaSuccess) return fail(TP_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
+    return fail(TP_ERR_CUDA);
+  const int t = cfg.t, H = cfg.hidden, d = cfg.head_dim, nq = cfg.q_heads_per_rank;
+  const int kvr = cfg.kv_heads_per_rank, Ipr = cfg.inter_per_rank;
+  MapUploader up;
+  if ((s = dev_alloc(m, &m->status, 256)) != TP_OK) return fail(s);
+  if (cudaMemsetAsync(m->status, 0, 256, st) != cudaSuccess) return fail(TP_ERR_CUDA);
+  if ((s = dev_alloc(m, &m->rope, (size_t)cfg.max_positions * (d / 2) * sizeof(float2))) != TP_OK)
+    return fail(s);
+  if (launch_rope_table(m->rope, cfg.max_positions, d, (double)cfg.rope_theta, st) != cudaSuccess)
+    return fail(TP_ERR_CUDA);
+
+  auto kv_head_of = [&](int r, int local) {
+    return cfg.kv_replicas == 1 ? r * kvr + local : r / cfg.kv_replicas;
+  };
+  // position inside a RoPE head of shard row w: the two halves of pair j sit at 2j, 2j+1
+  auto rope_src = [&](int w_) { return (w_ & 1) ? (w_ >> 1) + d / 2 : (w_ >> 1); };
+
+  m->layers.resize(cfg.n_layers);
+  for (int l = 0; l < cfg.n_layers; ++l) {
+    const tp_layer_weights_t& Wl = w->layers[l];
+    LayerShards& Ls = m->layers[l];
+    const int nqkv = (nq + 2 * kvr) * d;
+    if ((s = alloc_linear(m, &Ls.qkv, nqkv, H)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.gate_up, 2 * Ipr, H)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.o, H, nq * d)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.down, H, Ipr)) != TP_OK) return fail(s);
+    for (int r = 0; r < t; ++r) {
+      // qkv: [its Q heads | its KV heads] with RoPE pairs adjacent; V in natural order
+      std::vector<int32_t> mq(nq * d), mk(kvr * d), mv(kvr * d);
+      for (int hl = 0; hl < nq; ++hl)
+        for (int w_ = 0; w_ < d; ++w_) mq[hl * d + w_] = (r * nq + hl) * d + rope_src(w_);
+      for (int kl = 0; kl < kvr; ++kl)
+        for (int w_ = 0; w_ < d; ++w_) {
+          mk[kl * d + w_] = kv_head_of(r, kl) * d + rope_src(w_);
+          mv[kl * d + w_] = kv_head_of(r, kl) * d + w_;
+        }
+      int32_t *dq, *dk, *dv;
+      if ((s = up.upload(mq, &dq, st)) != TP_OK || (s = up.upload(mk, &dk, st)) != TP_OK ||
+          (s = up.upload(mv, &dv, st)) != TP_OK)
+        return fail(s);
+      uint16_t* base = Ls.qkv.data + (size_t)r * nqkv * H;
+      if (launch_copy_rows(base, H, Wl.wq, H, dq, nq * d, H, st) != cudaSuccess ||
+          launch_copy_rows(base + (size_t)nq * d * H, H, Wl.wk, H, dk, kvr * d, H, st) != cudaSuccess ||
+          launch_copy_rows(base + (size_t)(nq + kvr) * d * H, H, Wl.wv, H, dv, kvr * d, H, st) !=
+              cudaSuccess)
+        return fail(TP_ERR_CUDA);
+      // gate_up: row 2j = gate row r*Ipr + j, row 2j+1 = up row r*Ipr + j
+      std::vector<int32_t> mg(Ipr);
+      for (int j = 0; j < Ipr; ++j) mg[j] = r * Ipr + j;
+      int32_t* dg;
+      if ((s = up.upload(mg, &dg, st)) != TP_OK) return fail(s);
+      uint16_t* gbase = Ls.gate_up.data + (size_t)r * 2 * Ipr * H;
+      if (launch_copy_rows(gbase, 2 * H, Wl.wg, H, dg, Ipr, H, st) != cudaSuccess ||
+          launch_copy_rows(gbase + H, 2 * H, Wl.wu, H, dg, Ipr, H, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+    }
+    // row-parallel shards: columns [r K_r, (r+1) K_r) of wo / wd
+    std::vector<int32_t> ident(H);
+    for (int i = 0; i < H; ++i) ident[i] = i;
+    int32_t* di;
+    if ((s = up.upload(ident, &di, st)) != TP_OK) return fail(s);
+    for (int r = 0; r < t; ++r) {
+      if (launch_copy_rows(Ls.o.data + (size_t)r * H * nq * d, nq * d, Wl.wo + (size_t)r * nq * d,
+                           (int64_t)cfg.n_heads * d, di, H, nq * d, st) != cudaSuccess ||
+          launch_copy_rows(Ls.down.data + (size_t)r * H * Ipr, Ipr, Wl.wd + (size_t)r * Ipr,
+                           cfg.intermediate, di, H, Ipr, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+    }
+    if ((s = dev_alloc(m, &Ls.attn_norm, (size_t)H * 2)) != TP_OK ||
+        (s = dev_alloc(m, &Ls.mlp_norm, (size_t)H * 2)) != TP_OK)
+      return fail(s);
+    if (cudaMemcpyAsync(Ls.attn_norm, Wl.attn_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(Ls.mlp_norm, Wl.mlp_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+      return fail(TP_ERR_CUDA);
+  }
+  // vocab-parallel tables: padded to Vp rows, shard r = rows [r Vp/t, (r+1) Vp/t)
+  if (w->embed || w->lm_head) {
+    std::vector<int32_t> mv(cfg.vocab_padded);
+    for (int v = 0; v < cfg.vocab_padded; ++v) mv[v] = v < cfg.vocab ? v : -1;
+    int32_t* dmv;
+    if ((s = up.upload(mv, &dmv, st)) != TP_OK) return fail(s);
+    if (w->embed) {
+      if ((s = dev_alloc(m, &m->embed, (size_t)cfg.vocab_padded * H * 2)) != TP_OK) return fail(s);
+      if (launch_copy_rows(m->embed, H, w->embed, H, dmv, cfg.vocab_padded, H, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+    }
+    if (w->lm_head) {
+      if ((s = alloc_linear(m, &m->lm, cfg.vocab_per_rank, H)) != TP_OK) return fail(s);
+      if (launch_copy_rows(m->lm.data, H, w->lm_head, H, dmv, cfg.vocab_padded, H, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+    }
+  }
+  if (w->final_norm) {
+    if ((s = dev_alloc(m, &m->final_norm, (size_t)H * 2)) != TP_OK) return fail(s);
+    if (cudaMemcpyAsync(m->final_norm, w->final_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess)
+      return fail(TP_ERR_CUDA);
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(TP_ERR_CUDA);
+  *out = m;
+  return TP_OK;
+}
+
+size_t tp_workspace_bytes(const tp_model* m, int32_t max_tokens) {
+  if (!m || max_tokens < 0) return 0;
+  return ws_layout(m, std::max(max_tokens, 1)).total;
+}
+
+tp_status tp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return TP_ERR_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
+                           int32_t M, tp_bf16* y, int64_t y_rank_stride, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!valid_layer(m, layer) || (which != TP_QKV && which != TP_GATE_UP) || M < 0) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || y_rank_stride % 8) return TP_ERR_ARG;
+  const ShardedLinear& W = which == TP_QKV ? m->layers[layer].qkv : m->layers[layer].gate_up;
+  if (y_rank_stride < (int64_t)M * W.rows) return TP_ERR_ARG;
+  if (!ws_ok(m, M, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  EpiArgs e = base_epi(m, M);
+  e.out = y;
+  e.ld_out = W.rows;
+  e.out_group_stride = y_rank_stride;
+  e.which = which == TP_QKV ? 0 : 1;
+  return run_column(m, W, x, m->cfg.hidden, M, EPI_PLAIN, e, ws, ws_layout(m, M),
+                    static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_row_linear_reduce(const tp_model* m, int32_t layer, int32_t which,
+                               const tp_bf16* x, int64_t x_rank_stride, int64_t ldx, int32_t M,
+                               const tp_bf16* residual, tp_bf16* y, int32_t fused, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (!valid_layer(m, layer) || (which != TP_O && which != TP_DOWN) || M < 0) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  const ShardedLinear& W = which == TP_O ? m->layers[layer].o : m->layers[layer].down;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      x_rank_stride % 8 || ldx % 8 || ldx < W.cols)
+    return TP_ERR_ARG;
+  if (!ws_ok(m, M, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  return run_row(m, W, x, x_rank_stride, ldx, M, residual, y, fused, ws, ws_layout(m, M),
+                 static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_vocab_embed(const tp_model* m, const int32_t* ids, int32_t M, tp_bf16* h,
+                         void* stream) {
+  if (!m || M < 0) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!m->embed || !ids || !h || !aligned16(h)) return TP_ERR_ARG;
+  m->stats.kernel_launches++;
+  m->stats.allreduces++;
+  m->stats.allreduce_payload_bytes += (int64_t)M * m->cfg.hidden * 2;
+  return cuda_status(launch_embed(m->embed, m->cfg.vocab, m->cfg.vocab_per_rank, m->cfg.t, ids, M,
+                                  m->cfg.hidden, h, m->status, static_cast<cudaStream_t>(stream)));
+}
+
+static void count_gather(const tp_model* m, int S) {
+  m->stats.allgathers++;
+  const tp_config_t& c = m->cfg;
+  m->stats.allgather_recv_bytes_per_rank +=
+      (int64_t)S * ((int64_t)(c.t - 1) * c.vocab * 2 / c.t);
+}
+
+tp_status tp_lm_head_gather(const tp_model* m, const tp_bf16* x, int32_t S, tp_bf16* logits,
+                            int64_t ld_logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!m || S < 0) return TP_ERR_ARG;
+  if (S == 0) return TP_OK;
+  if (!m->lm.data || !x || !logits || !aligned16(x) || ld_logits < m->cfg.vocab) return TP_ERR_ARG;
+  if (!ws_ok(m, S, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  EpiArgs e = base_epi(m, S);
+  e.out = logits;
+  e.ld_out = ld_logits;
+  count_gather(m, S);
+  return run_column(m, m->lm, x, m->cfg.hidden, S, EPI_LOGITS, e, ws, ws_layout(m, S),
+                    static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_rmsnorm(const tp_model* m, const tp_bf16* x, const tp_bf16* w, int32_t M,
+                     tp_bf16* y, void* stream) {
+  if (!m || M < 0) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return TP_ERR_ARG;
+  m->stats.kernel_launches++;
+  return cuda_status(launch_rmsnorm(x, m->cfg.hidden, nullptr, w, M, m->cfg.hidden,
+                                    m->cfg.rms_eps, y, m->cfg.hidden,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+static tp_status check_batch(const tp_model* m, const tp_batch_t* b) {
+  if (!b || b->n_seqs < 1 || b->n_tokens < 1 || !b->positions || !b->token_seq || !b->k_cache ||
+      !b->v_cache || b->l_max < 1 || b->max_ctx < 1 || b->max_ctx > b->l_max ||
+      b->max_ctx > m->cfg.max_positions || b->l_max > m->cfg.max_positions)
+    return TP_ERR_ARG;
+  if (b->mode == TP_DECODE) {
+    if (b->n_tokens != b->n_seqs) return TP_ERR_ARG;
+  } else if (b->mode == TP_PREFILL) {
+    if (!b->seq_start || b->max_q_per_seq < 1) return TP_ERR_ARG;
+  } else {
+    return TP_ERR_ARG;
+  }
+  return TP_OK;
+}
+
+static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b, uint16_t* h,
+                               int fused, void* ws, const WsLayout& L, cudaStream_t st) {
+  const tp_config_t& c = m->cfg;
+  const LayerShards& Ls = m->layers[layer];
+  const int M = b->n_tokens, H = c.hidden, d = c.head_dim;
+  const int nhd = c.n_heads * d;
+  uint16_t* u = at<uint16_t>(ws, L.u);
+  uint16_t* q = at<uint16_t>(ws, L.q);
+  uint16_t* o = at<uint16_t>(ws, L.o);
+  uint16_t* act = at<uint16_t>(ws, L.act);
+  uint16_t* kc = b->k_cache[layer];
+  uint16_t* vc = b->v_cache[layer];
+  if (!kc || !vc || !aligned16(kc) || !aligned16(vc)) return TP_ERR_ARG;
+  tp_status s;
+  // u = RMSNorm(h)
+  m->stats.kernel_launches++;
+  TP_CHECK_CUDA(launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st));
+  // qkv (column-parallel) + RoPE + K/V into the rank caches
+  EpiArgs e = base_epi(m, M);
+  e.out = q;
+  e.ld_out = nhd;
+  e.k_cache = kc;
+  e.v_cache = vc;
+  e.kv_copy_stride = (int64_t)b->n_seqs * c.kv_heads_per_rank * b->l_max * d;
+  e.n_seqs = b->n_seqs;
+  e.l_max = b->l_max;
+  e.positions = b->positions;
+  e.token_seq = b->token_seq;
+  e.rope = m->rope;
+  if ((s = run_column(m, Ls.qkv, u, H, M, EPI_QKV, e, ws, L, st)) != TP_OK) return s;
+  // attention
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  const uint64_t slices = (uint64_t)c.kv_copies * b->n_seqs * c.kv_heads_per_rank;
+  if (!make_tmap(&a.tmK, kc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64) ||
+      !make_tmap(&a.tmV, vc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64))
+    return TP_ERR_CUDA;
+  a.q = q;
+  a.ld_q = nhd;
+  a.o = o;
+  a.ld_o = nhd;
+  a.positions = b->positions;
+  a.seq_start = b->seq_start;
+  a.n_seqs = b->n_seqs;
+  a.n_heads = c.n_heads;
+  a.n_kv = c.n_kv_heads;
+  a.head_dim = d;
+  a.kv_r = c.kv_heads_per_rank;
+  a.group = c.n_heads / c.n_kv_heads;
+  a.l_max = b->l_max;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  a.status = m->status;
+  m->stats.kernel_launches++;
+  if (b->mode == TP_DECODE) {
+    a.tiles_per_bg = cdiv(b->max_ctx, 64);
+    a.total_units = (int64_t)b->n_seqs * c.n_kv_heads * a.tiles_per_bg;
+    a.grid = (int)std::min<int64_t>(m->num_sms, a.total_units);
+    a.partials = at<float>(ws, L.attn_partials);
+    a.tickets = at<int>(ws, L.attn_tickets);
+    TP_CHECK_CUDA(launch_attn_decode(a, st));
+  } else {
+    TP_CHECK_CUDA(launch_attn_prefill(a, cdiv(b->max_q_per_seq, 64), st));
+  }
+  // o_proj (row-parallel) + reduction ① + residual
+  if ((s = run_row(m, Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st)) != TP_OK)
+    return s;
+  // u = RMSNorm(h); gate_up (column-parallel) + SiLU(gate) * up
+  m->stats.kernel_launches++;
+  TP_CHECK_CUDA(launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st));
+  EpiArgs e2 = base_epi(m, M);
+  e2.out = act;
+  e2.ld_out = c.intermediate;
+  if ((s = run_column(m, Ls.gate_up, u, H, M, EPI_SILU, e2, ws, L, st)) != TP_OK) return s;
+  // down_proj (row-parallel) + reduction ② + residual
+  return run_row(m, Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws, L, st);
+}
+
+tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                           tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!valid_layer(m, layer) || !h_inout || !aligned16(h_inout)) return TP_ERR_ARG;
+  tp_status s = check_batch(m, b);
+  if (s != TP_OK) return s;
+  if (!ws_ok(m, b->n_tokens, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  return layer_forward(m, layer, b, h_inout, fused, ws, ws_layout(m, b->n_tokens),
+                       static_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
+                     tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!m || !ids || !h || !logits || !aligned16(h)) return TP_ERR_ARG;
+  if (!m->embed || !m->lm.data || !m->final_norm) return TP_ERR_ARG;
+  tp_status s = check_batch(m, b);
+  if (s != TP_OK) return s;
+  if (!b->sample_rows || b->n_samples < 1 || ld_logits < m->cfg.vocab) return TP_ERR_ARG;
+  const int M = b->n_tokens;
+  if (!ws_ok(m, std::max(M, b->n_samples), ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(m, std::max(M, b->n_samples));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = tp_vocab_embed(m, ids, M, h, stream)) != TP_OK) return s;
+  for (int l = 0; l < m->cfg.n_layers; ++l)
+    if ((s = layer_forward(m, l, b, h, fused, ws, L, st)) != TP_OK) return s;
+  uint16_t* hs = at<uint16_t>(ws, L.hs);
+  m->stats.kernel_launches++;
+  TP_CHECK_CUDA(launch_rmsnorm(h, m->cfg.hidden, b->sample_rows, m->final_norm, b->n_samples,
+                               m->cfg.hidden, m->cfg.rms_eps, hs, m->cfg.hidden, st));
+  EpiArgs e = base_epi(m, b->n_samples);
+  e.out = logits;
+  e.ld_out = ld_logits;
+  count_gather(m, b->n_samples);
+  return run_column(m, m->lm, hs, m->cfg.hidden, b->n_samples, EPI_LOGITS, e, ws, L, st);
+}
+
+tp_status tp_get_stats(const tp_model* m, tp_stats_t* out) {
+  if (!m || !out) return TP_ERR_ARG;
+  *out = m->stats;
+  return TP_OK;
+}
+
+void tp_reset_stats(tp_model* m) {
+  if (m) memset(&m->stats, 0, sizeof(m->stats));
+}
+
+tp_status tp_check_device(tp_model* m, void* stream) {
+  if (!m) return TP_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TP_CHECK_CUDA(cudaStreamSynchronize(st));
+  int v = 0;
+  TP_CHECK_CUDA(cudaMemcpy(&v, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+  TP_CHECK_CUDA(cudaMemset(m->status, 0, sizeof(int)));
+  return static_cast<tp_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+symbol that include/tp.h declares, and applies the sharding rules of the pages
+through tp_config with the documented status codes."""
+import json
+import os
+import re
+
+import pytest
+
+import megatron_tensor_layers_tp_gb300.binding as B
+from megatron_tensor_layers_tp_gb300.runtime import make_config
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "tp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tp_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.lib()
+    declared = _declared_symbols()
+    assert "tp_layer_forward" in declared and len(declared) >= 15
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(B.exported_symbols()) == declared
+
+
+def _cfg(n_heads, n_kv, inter, vocab, t, hidden=None, head_dim=128):
+    hidden = hidden or n_heads * head_dim
+    return make_config(hidden, n_heads, n_kv, head_dim, inter, vocab, 1, t)
+
+
+def test_config_rules_match_the_golden_cases():
+    g = json.load(open(os.path.join(GOLDEN, "sharding_rules.json")))
+    for c in g["cases"]:
+        if c["t"] > 8:
+            continue  # outside the kernels' envelope; the rule itself is pinned in the oracle
+        inter = c["intermediate"]
+        cfg = _cfg(c["n_heads"], c["n_kv_heads"], inter, c["vocab"], c["t"],
+                   head_dim=64 if c["n_heads"] * 64 % 64 == 0 else 128)
+        st = B.tp_config(cfg)
+        if st == B.STATUS["TP_ERR_UNSUPPORTED"]:
+            # the rule fields are filled before the envelope check
+            pass
+        else:
+            assert st == B.TP_OK, (c, st)
+        assert (cfg.q_heads_per_rank, cfg.kv_heads_per_rank, cfg.kv_replicas, cfg.vocab_padded) == \
+            (c["q_per_rank"], c["kv_per_rank"], c["replicas"], c["vocab_padded"]), c
+        assert cfg.vocab_per_rank * c["t"] == cfg.vocab_padded
+        assert cfg.kv_copies == min(c["t"], c["n_kv_heads"])
+
+
+def test_config_rejections_have_the_named_status():
+    ST = B.STATUS
+    assert B.tp_config(_cfg(40, 8, 27648, 152064, 3)) == ST["TP_ERR_DIVISIBILITY"]     # n_h % t
+    assert B.tp_config(_cfg(32, 8, 14337, 128256, 2)) == ST["TP_ERR_DIVISIBILITY"]     # I % t
+    assert B.tp_config(_cfg(48, 12, 1536, 1000, 8)) == ST["TP_ERR_KV_REPLICA"]         # n_kv % t
+    assert B.tp_config(_cfg(8, 3, 1536, 1000, 2)) == ST["TP_ERR_DIVISIBILITY"]         # GQA groups
+    assert B.tp_config(_cfg(20, 4, 1280, 1000, 10)) == ST["TP_ERR_KV_REPLICA"]         # t % n_kv
+    assert B.tp_config(_cfg(32, 8, 14336, 128256, 16)) == ST["TP_ERR_UNSUPPORTED"]     # t > 8
+    assert B.tp_config(_cfg(32, 8, 14336, 128256, 0)) == ST["TP_ERR_ARG"]
+    bad = _cfg(32, 8, 14336, 128256, 2, head_dim=96)
+    assert B.tp_config(bad) == ST["TP_ERR_UNSUPPORTED"]
+    ok = _cfg(32, 8, 14336, 128256, 8)
+    assert B.tp_config(ok) == B.TP_OK
+    assert (ok.q_heads_per_rank, ok.kv_heads_per_rank, ok.inter_per_rank, ok.vocab_per_rank) == \
+        (4, 1, 1792, 16032)
+
+
+def test_calls_without_a_model_are_rejected_on_the_host():
+    ST = B.STATUS
+    assert B.tp_workspace_bytes(None, 16) == 0
+    assert B.tp_column_linear(None, 0, 0, 0, 16, 0, 0, 0, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.tp_row_linear_reduce(None, 0, 2, 0, 0, 0, 16, 0, 0, 1, 0, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.tp_vocab_embed(None, 0, 4, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.tp_lm_head_gather(None, 0, 1, 0, 0, 0, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.tp_rmsnorm(None, 0, 0, 1, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.lib().tp_get_stats(None, None) == ST["TP_ERR_ARG"]
+    for code, name in B.STATUS_NAMES.items():
+        assert B.strerror(code) and B.strerror(code) != "unknown status", name

@@ -1,0 +1,184 @@
+"""Decoder-layer and full-forward parity of the CUDA path against the oracle at
+sizes the oracle finishes in seconds (several tiles, ragged tails, KV
+replication), plus GPU-side invariants: sharded vs unsharded (t vs t=1),
+decode step vs prefill row, determinism and the collective counters."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle as O  # noqa: E402
+import synth  # noqa: E402
+from megatron_tensor_layers_tp_gb300 import binding as B  # noqa: E402
+from megatron_tensor_layers_tp_gb300.runtime import Batch  # noqa: E402
+from tests.parity_utils import (build_model, make_batch, oracle_batch, oracle_caches,  # noqa: E402
+                                oracle_dims, oracle_layer, rel_err, to_f64)
+
+LAYER_TOL = 2e-2
+LOGIT_TOL = 5e-2
+
+
+def _wl(mode, n_seqs, seq_len, ctx, hidden=512, n_heads=8, n_kv=2, head_dim=64, inter=1536,
+        vocab=1001, layers=1, embed=False, norm_sigma=0.1):
+    return synth.Workload(f"unit-{mode}", hidden, n_heads, n_kv, head_dim, inter, vocab, layers, (1,),
+                          mode, n_seqs, seq_len, ctx, embed, seed=4, norm_weight_sigma=norm_sigma)
+
+
+def _run_layer(w, t, fused=True):
+    model, _, _ = build_model(w, t)
+    batch, caches = make_batch(model, w)
+    h = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
+    synth.fill_normal_(h, w.seed, synth.tensor_id("hidden"), w.sigma_h)
+    model.layer_forward(0, batch, h, fused=fused)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    return model, h, caches
+
+
+def _oracle_layer(w):
+    dims = oracle_dims(w)
+    h = synth.host_hidden(w)
+    kc, vc = oracle_caches(w, 0, range(w.n_seqs))
+    out = O.layer_forward(h, oracle_layer(w, 0), kc, vc, oracle_batch(w), dims)
+    return out, kc, vc
+
+
+def _cache_logical(model, cache, w):
+    """library layout [copies, seqs, kv_r, L, d] -> logical {b: [n_kv, L, d]}"""
+    c = model.cfg
+    arr = to_f64(cache)
+    return {b: arr[:, b].reshape(c.kv_copies * c.kv_heads_per_rank, w.l_max, w.head_dim)
+            for b in range(w.n_seqs)}
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+@pytest.mark.parametrize("n_kv", [8, 2, 1])
+@pytest.mark.parametrize("fused", [True, False])
+def test_decode_layer_matches_oracle(t, n_kv, fused):
+    w = _wl("decode", n_seqs=5, seq_len=1, ctx=150, n_kv=n_kv)
+    model, h, (ks, vs) = _run_layer(w, t, fused)
+    ref, kc, vc = _oracle_layer(w)
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    # the new token's K/V landed in the rank caches at position ctx-1
+    gk = _cache_logical(model, ks[0], w)
+    for b in range(w.n_seqs):
+        assert rel_err(gk[b][:, w.ctx - 1], kc[b][:, w.ctx - 1]) <= LAYER_TOL
+        assert np.array_equal(gk[b][:, : w.ctx - 1], kc[b][:, : w.ctx - 1])
+    model.close()
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+@pytest.mark.parametrize("head_dim,n_heads,n_kv", [(64, 8, 2), (128, 4, 4)])
+def test_prefill_layer_matches_oracle(t, head_dim, n_heads, n_kv):
+    w = _wl("prefill", n_seqs=3, seq_len=70, ctx=70, head_dim=head_dim, n_heads=n_heads, n_kv=n_kv)
+    model, h, (ks, vs) = _run_layer(w, t)
+    ref, kc, vc = _oracle_layer(w)
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    gv = _cache_logical(model, vs[0], w)
+    for b in range(w.n_seqs):
+        assert rel_err(gv[b], vc[b]) <= LAYER_TOL
+    model.close()
+
+
+def test_ragged_prefill_matches_oracle():
+    w = _wl("prefill", n_seqs=3, seq_len=70, ctx=70)
+    lens = [5, 70, 33]
+    model, _, _ = build_model(w, 2, max_tokens=sum(lens))
+    ks = [model.alloc_kv(3, 70)]
+    vs = [model.alloc_kv(3, 70)]
+    from tests.parity_utils import fill_device_kv
+    fill_device_kv(model, w, ks[0], "k_cache", 0)
+    fill_device_kv(model, w, vs[0], "v_cache", 0)
+    pos = np.concatenate([np.arange(n) for n in lens]).astype(np.int32)
+    seq = np.concatenate([np.full(n, b) for b, n in enumerate(lens)]).astype(np.int32)
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    M = sum(lens)
+    batch = Batch(B.TP_PREFILL, 3, M, max(lens), max(lens), 70, torch.from_numpy(pos).cuda(),
+                  torch.from_numpy(seq).cuda(), torch.from_numpy(start).cuda(), ks, vs, None)
+    hx = synth.normal_f64(4, 555, (M, w.hidden), 1.0)
+    h = torch.from_numpy(hx.astype(np.float32)).to(torch.bfloat16).cuda()
+    model.layer_forward(0, batch, h)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    kc, vc = oracle_caches(w, 0, range(3))
+    ref = O.layer_forward(hx, oracle_layer(w, 0), kc, vc, O.Batch(seq, pos), oracle_dims(w))
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    model.close()
+
+
+def test_sharded_equals_unsharded_on_gpu():
+    w = _wl("decode", n_seqs=16, seq_len=1, ctx=300, hidden=1024, n_heads=16, n_kv=8, head_dim=64,
+            inter=2048)
+    outs = {}
+    for t in (1, 2, 4, 8):
+        model, h, _ = _run_layer(w, t)
+        outs[t] = to_f64(h)
+        model.close()
+    for t in (2, 4, 8):
+        assert rel_err(outs[t], outs[1]) <= 1e-2, t
+
+
+def test_decode_step_equals_last_prefill_row_on_gpu():
+    L = 90
+    wp = _wl("prefill", n_seqs=2, seq_len=L, ctx=L)
+    model, _, _ = build_model(wp, 2, max_tokens=2 * L)
+    batch, (ks, vs) = make_batch(model, wp)
+    h = torch.empty((2 * L, wp.hidden), dtype=torch.bfloat16, device="cuda")
+    synth.fill_normal_(h, 8, 8, 1.0)
+    h_in = h.clone()
+    model.layer_forward(0, batch, h)
+    # decode the last token of each sequence against the cache the prefill wrote
+    kd, vd = ks[0].clone(), vs[0].clone()
+    kd[:, :, :, L - 1] = 0
+    vd[:, :, :, L - 1] = 0
+    from megatron_tensor_layers_tp_gb300.runtime import decode_batch
+    db = decode_batch(2, L, [kd], [vd], L)
+    hd = h_in[[L - 1, 2 * L - 1]].contiguous()
+    model.layer_forward(0, db, hd)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(hd), to_f64(h[[L - 1, 2 * L - 1]])) <= 1e-2
+    model.close()
+
+
+def test_layer_is_deterministic():
+    w = _wl("decode", n_seqs=16, seq_len=1, ctx=500)
+    a_model, a, _ = _run_layer(w, 4)
+    b_model, b, _ = _run_layer(w, 4)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    a_model.close(); b_model.close()
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_tiny_forward_matches_oracle(t):
+    from tests.parity_utils import run_tiny_forward_check
+    assert run_tiny_forward_check(t) <= LOGIT_TOL
+
+
+def test_two_layer_forward_with_padded_vocab_and_counters():
+    w = _wl("decode", n_seqs=6, seq_len=1, ctx=40, vocab=1001, layers=2, embed=True)
+    t = 4
+    model, _, _ = build_model(w, t)
+    batch, _ = make_batch(model, w)
+    ids_np = synth.token_ids(w)
+    ids = torch.from_numpy(ids_np).cuda()
+    model.reset_stats()
+    logits = model.forward(ids, batch)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    st = model.stats()
+    assert st.allreduces == 2 * 2 + 1
+    assert st.allreduce_payload_bytes == (2 * 2 + 1) * w.tokens * w.hidden * 2
+    assert st.allgathers == 1
+    assert st.allgather_recv_bytes_per_rank == w.n_seqs * ((t - 1) * w.vocab * 2 // t)
+    dims = oracle_dims(w)
+    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
+    ob = oracle_batch(w)
+    for l in range(2):
+        kc, vc = oracle_caches(w, l, range(w.n_seqs))
+        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
+    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
+                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    assert logits.shape == (w.n_seqs, w.vocab)
+    assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
+    model.close()
