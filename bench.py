@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark: tensor-parallel Llama decoder layer, t ranks emulated on one GB300.
+
+One step = one decoder layer forward (RMSNorm, column-parallel qkv + RoPE +
+KV write, GQA attention, row-parallel o_proj with the fused t-way reduction,
+RMSNorm, column-parallel gate_up + SiLU, row-parallel down_proj with the fused
+reduction) of a decode batch: 16 sequences, each one new token attending to a
+1024-token KV cache, at the Llama-3.1-8B shape (hidden 4096, 32 Q / 8 KV heads,
+head_dim 128, intermediate 14336).  The headline runs t = 8 emulated ranks;
+t = 1, 2, 4 are reported beside it.  Seeded synthetic weights ~N(0, 0.02),
+KV cache ~N(0, 1), hidden ~N(0, 1).  Steps rotate over 4 layers with distinct
+weights and caches (2 GB), so every step streams inputs far larger than L2.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sharded-layer tokens/s at Llama-3.1-8B shape, t=1..8; % of HBM/TC roofline"
+UNIT = "tokens/s"
+WORKLOAD = "llama8b_decode"
+LAYER_KINDS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--t", type=int, default=8)
+    p.add_argument("--rotate", type=int, default=4)
+    p.add_argument("--fused", type=int, default=1)
+    p.add_argument("--per-t", type=int, default=1)
+    p.add_argument("--cpu-baseline", type=int, default=1)
+    p.add_argument("--cpu-budget-s", type=float, default=15.0)
+    p.add_argument("--reference-budget-s", type=float, default=150.0)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic: what the method must move once per step)
+# ---------------------------------------------------------------------------
+def layer_bytes(w, t):
+    H, d, I = w.hidden, w.head_dim, w.intermediate
+    nkv_r = w.n_kv_heads // t if w.n_kv_heads >= t else 1
+    nq_r = w.n_heads // t
+    M = w.tokens
+    b = {
+        "gemm_qkv": t * (nq_r + 2 * nkv_r) * d * H * 2 + M * H * 2 + M * (w.n_heads + 2 * w.n_kv_heads) * d * 2,
+        "gemm_o": H * w.n_heads * d * 2 + M * w.n_heads * d * 2 + 2 * M * H * 2,
+        "gemm_gate_up": 2 * I * H * 2 + M * H * 2 + M * I * 2,
+        "gemm_down": H * I * 2 + M * I * 2 + 2 * M * H * 2,
+        "attn_decode": w.n_seqs * w.n_kv_heads * w.ctx * d * 2 * 2 + 2 * M * w.n_heads * d * 2,
+        "rmsnorm": 2 * M * H * 2 + H * 2,
+    }
+    total = sum(b.values()) + b["rmsnorm"]  # two norms per layer
+    return b, total
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk.get("hbm_gbs", 6800.0), pk.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for ts, s in self.samples if t0 <= ts <= t1]
+        adjacent = False
+        if not inside:
+            near = sorted(self.samples, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:3]
+            inside = [s for _, s in near]
+            adjacent = True
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in inside:
+            for name, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": num(inside[0][2]), "reasons": sorted(reasons),
+               "power_w_max": max((num(s[3]) or 0) for s in inside), "samples": len(inside)}
+        if adjacent:
+            out["sampled_adjacent"] = True
+        return out
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def build(w, t, rotate):
+    import torch
+    import synth
+    from megatron_tensor_layers_tp_gb300.runtime import TPModel, decode_batch, make_config
+    cfg = make_config(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab,
+                      rotate, t, w.rms_eps, w.rope_theta, max_positions=w.l_max)
+    layers = []
+    for l in range(rotate):
+        shapes = synth.weight_shapes(w, l)
+        L = {}
+        for k in LAYER_KINDS:
+            x = torch.empty(shapes[k], dtype=torch.bfloat16, device="cuda")
+            if k.endswith("norm"):
+                x.fill_(1.0)
+            else:
+                synth.fill_normal_(x, w.seed, synth.tensor_id(k, l), w.sigma_w)
+            L[k] = x
+        layers.append(L)
+    model = TPModel(cfg, layers, max_tokens=w.tokens)
+    del layers
+    torch.cuda.empty_cache()
+    ks, vs = [], []
+    for l in range(rotate):
+        k = model.alloc_kv(w.n_seqs, w.l_max)
+        v = model.alloc_kv(w.n_seqs, w.l_max)
+        for cache, kind in ((k, "k_cache"), (v, "v_cache")):
+            for cp in range(cfg.kv_copies):
+                for b in range(w.n_seqs):
+                    synth.fill_normal_(cache[cp, b], w.seed, synth.tensor_id(kind, l), w.sigma_kv,
+                                       start=synth.kv_logical_start(w, b, cp * cfg.kv_heads_per_rank))
+        ks.append(k)
+        vs.append(v)
+    batch = decode_batch(w.n_seqs, w.ctx, ks, vs, w.l_max)
+    h = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
+    synth.fill_normal_(h, w.seed, synth.tensor_id("hidden"), w.sigma_h)
+    torch.cuda.synchronize()
+    return model, batch, h
+
+
+def timed_steps(model, batch, h, steps, warmup, rotate, fused, stream, profile=False):
+    import torch
+    from megatron_tensor_layers_tp_gb300 import binding as B
+    cb = batch.to_c()
+    ws, nws = model.ws_args
+    s = stream.cuda_stream
+
+    def step(i):
+        B.check(B.tp_layer_forward(model.handle, i % rotate, cb, h.data_ptr(), fused, ws, nws, s),
+                "tp_layer_forward")
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    B.tp_profile(model.handle, profile)
+    model.reset_stats()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    B.tp_profile(model.handle, False)
+    ms = e0.elapsed_time(e1)
+    prof = B.tp_profile_read(model.handle, s) if profile else {}
+    launches = model.stats().kernel_launches
+    return ms, prof, launches
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import synth
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    w = synth.WORKLOADS[WORKLOAD]
+    stream = torch.cuda.Stream()
+    hbm_peak, tc_peak, peak_src = read_peaks()
+    with torch.cuda.stream(stream):
+        model, batch, h = build(w, args.t, args.rotate)
+    gpu_idx = int(os.environ.get("LOCAL_RANK", 0))
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_idx = int(vis.split(",")[gpu_idx])
+        except ValueError:
+            pass
+    sampler = ClockSampler(gpu_idx)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    ms, prof, launches = timed_steps(model, batch, h, args.steps, args.warmup, args.rotate,
+                                     args.fused, stream, profile=True)
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    if world > 1:
+        tm = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    assert model.check_device(stream) == 0, "device status word set"
+    ms_step = ms / args.steps
+    tokens = w.tokens
+    value = world * tokens * args.steps / (ms / 1e3)
+
+    kb, step_bytes = layer_bytes(w, args.t)
+    kernels = {}
+    for name, (n, tot) in prof.items():
+        avg = tot / n
+        entry = {"launches": n, "avg_us": round(avg * 1e3, 2),
+                 "share": None}
+        if name in kb:
+            entry["gbs"] = round(kb[name] / (avg * 1e-3) / 1e9, 1)
+            entry["frac_hbm"] = round(entry["gbs"] / hbm_peak, 3)
+        kernels[name] = entry
+    tot_all = sum(tot for _, tot in prof.values()) or 1.0
+    for name, (n, tot) in prof.items():
+        kernels[name]["share"] = round(tot / tot_all, 3)
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    roofline = None
+    if dom in kb:
+        n, tot = prof[dom]
+        avg_s = tot / n * 1e-3
+        ach = kb[dom] / avg_s / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(ach / hbm_peak, 3), "traffic": None,
+                    "algorithmic_bytes": kb[dom], "peak_source": peak_src}
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+
+    # t = 1, 2, 4 beside the headline
+    per_t = {}
+    if args.per_t and rank == 0 and world == 1:
+        per_t[str(args.t)] = {"tokens_per_s": round(value, 1), "ms_per_step": round(ms_step, 4),
+                              "step_hbm_frac": round(step_gbs / hbm_peak, 3)}
+        for tt in (1, 2, 4):
+            if tt == args.t:
+                continue
+            with torch.cuda.stream(stream):
+                m2, b2, h2 = build(w, tt, args.rotate)
+            ms2, _, _ = timed_steps(m2, b2, h2, max(args.steps // 4, 20), args.warmup, args.rotate,
+                                    args.fused, stream)
+            st2 = ms2 / max(args.steps // 4, 20)
+            _, sb2 = layer_bytes(w, tt)
+            per_t[str(tt)] = {"tokens_per_s": round(tokens / (st2 * 1e-3), 1),
+                              "ms_per_step": round(st2, 4),
+                              "step_hbm_frac": round(sb2 / (st2 * 1e-3) / 1e9 / hbm_peak, 3)}
+            m2.close()
+            del m2, b2, h2
+        # the unfused reduction variant at the headline t
+        ms_u, _, _ = timed_steps(model, batch, h, max(args.steps // 4, 20), args.warmup,
+                                 args.rotate, 0, stream)
+        per_t[f"{args.t}_unfused"] = {
+            "tokens_per_s": round(tokens / (ms_u / max(args.steps // 4, 20) * 1e-3), 1),
+            "ms_per_step": round(ms_u / max(args.steps // 4, 20), 4),
+            "extra_partial_bytes_per_row_op": 2 * args.t * w.tokens * w.hidden * 4}
+
+    # end to end through the public API: pinned host input -> device -> layer -> host
+    e2e_steps = max(min(args.steps, 500), 10)
+    hin = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, pin_memory=True)
+    hin.copy_(h.cpu())
+    hout = torch.empty_like(hin, pin_memory=True)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            h.copy_(hin, non_blocking=True)
+            model.layer_forward(i % args.rotate, batch, h, bool(args.fused), stream=stream)
+            hout.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    cb = batch.to_c()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            h.copy_(hin, non_blocking=True)
+            model.layer_forward(i % args.rotate, batch, h, bool(args.fused), stream=stream, cbatch=cb)
+            hout.copy_(h, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        tm = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms_e2e = float(tm.item())
+    e2e = {"value": round(world * tokens * e2e_steps / (ms_e2e / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": w.tokens * w.hidden * 2, "d2h_bytes_per_step": w.tokens * w.hidden * 2,
+           "steps": e2e_steps}
+
+    cpu = None
+    if args.cpu_baseline and rank == 0 and world == 1:
+        cpu = cpu_baseline(w, args.t, args.cpu_budget_s)
+
+    model.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded random-init weights ~N(0,0.02), KV cache ~N(0,1), hidden ~N(0,1)",
+        "config": {
+            "workload": "Llama-3.1-8B-shaped decoder layer, decode: 16 sequences x 1 token, "
+                        "1024-token KV context, t emulated TP ranks on one GPU",
+            "hidden": w.hidden, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "intermediate": w.intermediate, "batch": w.n_seqs,
+            "ctx": w.ctx, "t": args.t, "fused_reduction": bool(args.fused),
+            "parallelism": f"tp{args.t} emulated on 1 GPU" + (f", {world} replicas" if world > 1 else ""),
+            "l2": f"inputs larger than L2: steps rotate over {args.rotate} layers with distinct "
+                  f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
+            "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
+            "step_hbm_frac": round(step_gbs / hbm_peak, 3),
+            "per_t": per_t, "kernels": kernels,
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_inputs(w):
+    import oracle as O
+    import synth
+    shapes = synth.weight_shapes(w, 0)
+    W = O.LayerWeights(**{k: synth.host_weight(w, k, 0, shapes[k]) for k in LAYER_KINDS})
+    h = synth.host_hidden(w)
+    kc = {b: synth.host_kv(w, "k_cache", 0, b) for b in range(w.n_seqs)}
+    vc = {b: synth.host_kv(w, "v_cache", 0, b) for b in range(w.n_seqs)}
+    dims = O.Dims(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab,
+                  w.rms_eps, w.rope_theta)
+    return W, h, kc, vc, dims
+
+
+def oracle_step(w, t, inputs):
+    import oracle as O
+    W, h, kc, vc, dims = inputs
+    p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)
+    return O.sharded_layer_forward(h, W, O.split_cache_copies(kc, dims, p),
+                                   O.split_cache_copies(vc, dims, p),
+                                   O.Batch.decode(w.n_seqs, w.ctx), dims, p)
+
+
+def cpu_baseline(w, t, budget_s):
+    inputs = oracle_inputs(w)
+    oracle_step(w, t, inputs)  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(w, t, inputs)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(n * w.tokens / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} decode step(s) of one layer, {w.tokens} tokens, t={t} sharded emulation "
+                      f"in float64 numpy ({dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    inputs = oracle_inputs(w)
+    for _ in range(min(args.warmup, 2)):
+        oracle_step(w, args.t, inputs)
+    n, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, args.t, inputs)
+        n += 1
+        if time.perf_counter() - t0 >= args.reference_budget_s:
+            break
+    dt = time.perf_counter() - t0
+    value = n * w.tokens / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "steps_run": n, "warmup": args.warmup,
+        "ms_per_step": round(dt / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
+        "config": {"workload": "Llama-3.1-8B-shaped decoder layer, decode: 16 sequences x 1 token, "
+                               "1024-token KV context, t emulated TP ranks", "t": args.t},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} decode step(s) of {w.tokens} tokens (wall-time capped at "
+                                   f"{args.reference_budget_s:.0f} s)"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

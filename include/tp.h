@@ -260,6 +260,21 @@ typedef struct {
 tp_status tp_get_stats(const tp_model* m, tp_stats_t* out);
 void tp_reset_stats(tp_model* m);
 
+/* Per-kernel timing.  While enabled, every launch the library makes is
+ * bracketed by two CUDA events recorded on the launch stream (at most 16384
+ * launches are recorded between two reads).  tp_profile_read synchronises
+ * `stream`, sums the elapsed times per kernel name into `out` (up to `max`
+ * entries, count in *n) and clears the records. */
+typedef struct {
+  char name[24];
+  int64_t launches;
+  double total_ms;
+} tp_kernel_time_t;
+
+tp_status tp_profile(tp_model* m, int32_t enable);
+tp_status tp_profile_read(tp_model* m, void* stream, tp_kernel_time_t* out, int32_t max,
+                          int32_t* n);
+
 /* Synchronises `stream`, returns the device status word (TP_OK,
  * TP_ERR_TOKEN_RANGE or TP_ERR_DEVICE_TIMEOUT) and clears it. */
 tp_status tp_check_device(tp_model* m, void* stream);

@@ -55,6 +55,10 @@ class tp_stats_t(Structure):
                                        "allgather_recv_bytes_per_rank", "kernel_launches")]
 
 
+class tp_kernel_time_t(Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", c_int64), ("total_ms", ctypes.c_double)]
+
+
 class TPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -89,6 +93,9 @@ _SIGS = {
     "tp_reset_stats": (None, [c_void_p]),
     "tp_check_device": (c_int32, [c_void_p, c_void_p]),
     "tp_strerror": (c_char_p, [c_int32]),
+    "tp_profile": (c_int32, [c_void_p, c_int32]),
+    "tp_profile_read": (c_int32, [c_void_p, c_void_p, POINTER(tp_kernel_time_t), c_int32,
+                                  POINTER(c_int32)]),
 }
 
 
@@ -201,3 +208,15 @@ def tp_reset_stats(model) -> None:
 
 def tp_check_device(model, stream) -> int:
     return lib().tp_check_device(model, stream)
+
+
+def tp_profile(model, enable: bool) -> int:
+    return lib().tp_profile(model, int(enable))
+
+
+def tp_profile_read(model, stream) -> dict:
+    """{kernel name: (launches, total_ms)} since the last read."""
+    arr = (tp_kernel_time_t * 64)()
+    n = c_int32()
+    check(lib().tp_profile_read(model, stream, arr, 64, ctypes.byref(n)), "tp_profile_read")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}

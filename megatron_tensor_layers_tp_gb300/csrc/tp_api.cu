@@ -41,6 +41,12 @@ struct tp_model {
   int* status = nullptr;
   std::vector<void*> allocs;
   mutable tp_stats_t stats;
+  // per-launch timing (tp_profile)
+  bool profiling = false;
+  struct Rec { const char* name; cudaEvent_t a, b; };
+  mutable std::vector<Rec> recs;
+  mutable std::vector<cudaEvent_t> pool;
+  mutable size_t pool_used = 0;
 };
 
 namespace {
@@ -107,6 +113,29 @@ tp_status cuda_status(cudaError_t e) {
     cudaError_t _e = (expr);                        \
     if (_e != cudaSuccess) return cuda_status(_e);  \
   } while (0)
+
+constexpr size_t kMaxProfiled = 16384;
+
+// Every kernel launch of the library goes through here: counted, and timed
+// with two events on the launch stream while profiling is enabled.
+template <class F>
+cudaError_t launch(const tp_model* m, const char* name, cudaStream_t st, F&& f) {
+  m->stats.kernel_launches++;
+  if (!m->profiling || m->recs.size() >= kMaxProfiled) return f();
+  while (m->pool.size() < m->pool_used + 2) {
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return e;
+    m->pool.push_back(ev);
+  }
+  cudaEvent_t a = m->pool[m->pool_used++], b = m->pool[m->pool_used++];
+  cudaError_t e = cudaEventRecord(a, st);
+  if (e != cudaSuccess) return e;
+  e = f();
+  if (e != cudaSuccess) return e;
+  m->recs.push_back({name, a, b});
+  return cudaEventRecord(b, st);
+}
 
 template <class T>
 tp_status dev_alloc(tp_model* m, T** p, size_t bytes) {
@@ -209,9 +238,9 @@ EpiArgs base_epi(const tp_model* m, int M) {
 
 // Column-parallel family (qkv, gate_up, LM head): each rank r produces its own
 // [M, rows] output from the replicated x [M, K].
-tp_status run_column(const tp_model* m, const ShardedLinear& W, const uint16_t* x, int64_t ldx,
-                     int M, int epi, const EpiArgs& e, void* ws, const WsLayout& L,
-                     cudaStream_t st) {
+tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W,
+                     const uint16_t* x, int64_t ldx, int M, int epi, const EpiArgs& e, void* ws,
+                     const WsLayout& L, cudaStream_t st) {
   if (M == 0) return TP_OK;
   const tp_config_t& c = m->cfg;
   const int K = W.cols;
@@ -253,14 +282,13 @@ tp_status run_column(const tp_model* m, const ShardedLinear& W, const uint16_t* 
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
   a.e = e;
-  m->stats.kernel_launches++;
-  return cuda_status(launch_gemm(p.swap, epi, a, p.smem, st));
+  return cuda_status(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
 }
 
 // Row-parallel family (o_proj, down_proj): rank r holds W_r [H, K_r] and reads
 // x_r [M, K_r]; fused = sum over ranks inside the GEMM (epilogue EPI_RESID),
 // otherwise per-rank fp32 partials then the ordered reduction kernel.
-tp_status run_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
+tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, const uint16_t* x,
                   int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
                   uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st) {
   if (M == 0) return TP_OK;
@@ -321,11 +349,11 @@ tp_status run_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
   }
   a.total_iters = (int64_t)a.n_groups * a.a_tiles * a.b_tiles * a.k_slices * a.k_iters_slice;
   a.grid = (int)std::min<int64_t>(m->num_sms, a.total_iters);
-  m->stats.kernel_launches++;
-  TP_CHECK_CUDA(launch_gemm(p.swap, epi, a, p.smem, st));
+  TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
   if (!fused) {
-    m->stats.kernel_launches++;
-    TP_CHECK_CUDA(launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, residual, y, st));
+    TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {
+      return launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, residual, y, st);
+    }));
   }
   m->stats.allreduces++;
   m->stats.allreduce_payload_bytes += (int64_t)M * H * 2;
@@ -448,8 +476,41 @@ tp_status tp_get_config(const tp_model* m, tp_config_t* out) {
 
 void tp_free(tp_model* m) {
   if (!m) return;
+  for (cudaEvent_t e : m->pool) cudaEventDestroy(e);
   for (void* p : m->allocs) cudaFree(p);
   delete m;
+}
+
+tp_status tp_profile(tp_model* m, int32_t enable) {
+  if (!m) return TP_ERR_ARG;
+  m->profiling = enable != 0;
+  return TP_OK;
+}
+
+tp_status tp_profile_read(tp_model* m, void* stream, tp_kernel_time_t* out, int32_t max,
+                          int32_t* n) {
+  if (!m || !n || (max > 0 && !out)) return TP_ERR_ARG;
+  TP_CHECK_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  std::vector<tp_kernel_time_t> agg;
+  for (const auto& r : m->recs) {
+    float ms = 0.f;
+    TP_CHECK_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+    size_t i = 0;
+    while (i < agg.size() && strncmp(agg[i].name, r.name, sizeof(agg[i].name)) != 0) ++i;
+    if (i == agg.size()) {
+      tp_kernel_time_t k;
+      memset(&k, 0, sizeof(k));
+      strncpy(k.name, r.name, sizeof(k.name) - 1);
+      agg.push_back(k);
+    }
+    agg[i].launches++;
+    agg[i].total_ms += ms;
+  }
+  m->recs.clear();
+  m->pool_used = 0;
+  *n = 0;
+  for (size_t i = 0; i < agg.size() && (int32_t)i < max; ++i) out[(*n)++] = agg[i];
+  return TP_OK;
 }
 
 tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void* stream,
@@ -607,7 +668,7 @@ tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, cons
   e.ld_out = W.rows;
   e.out_group_stride = y_rank_stride;
   e.which = which == TP_QKV ? 0 : 1;
-  return run_column(m, W, x, m->cfg.hidden, M, EPI_PLAIN, e, ws, ws_layout(m, M),
+  return run_column(m, "gemm_column", W, x, m->cfg.hidden, M, EPI_PLAIN, e, ws, ws_layout(m, M),
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -622,7 +683,7 @@ tp_status tp_row_linear_reduce(const tp_model* m, int32_t layer, int32_t which,
       x_rank_stride % 8 || ldx % 8 || ldx < W.cols)
     return TP_ERR_ARG;
   if (!ws_ok(m, M, ws, ws_bytes)) return TP_ERR_WORKSPACE;
-  return run_row(m, W, x, x_rank_stride, ldx, M, residual, y, fused, ws, ws_layout(m, M),
+  return run_row(m, "gemm_row", W, x, x_rank_stride, ldx, M, residual, y, fused, ws, ws_layout(m, M),
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -631,11 +692,13 @@ tp_status tp_vocab_embed(const tp_model* m, const int32_t* ids, int32_t M, tp_bf
   if (!m || M < 0) return TP_ERR_ARG;
   if (M == 0) return TP_OK;
   if (!m->embed || !ids || !h || !aligned16(h)) return TP_ERR_ARG;
-  m->stats.kernel_launches++;
   m->stats.allreduces++;
   m->stats.allreduce_payload_bytes += (int64_t)M * m->cfg.hidden * 2;
-  return cuda_status(launch_embed(m->embed, m->cfg.vocab, m->cfg.vocab_per_rank, m->cfg.t, ids, M,
-                                  m->cfg.hidden, h, m->status, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch(m, "vocab_embed", st, [&] {
+    return launch_embed(m->embed, m->cfg.vocab, m->cfg.vocab_per_rank, m->cfg.t, ids, M,
+                        m->cfg.hidden, h, m->status, st);
+  }));
 }
 
 static void count_gather(const tp_model* m, int S) {
@@ -655,7 +718,7 @@ tp_status tp_lm_head_gather(const tp_model* m, const tp_bf16* x, int32_t S, tp_b
   e.out = logits;
   e.ld_out = ld_logits;
   count_gather(m, S);
-  return run_column(m, m->lm, x, m->cfg.hidden, S, EPI_LOGITS, e, ws, ws_layout(m, S),
+  return run_column(m, "gemm_lm_head", m->lm, x, m->cfg.hidden, S, EPI_LOGITS, e, ws, ws_layout(m, S),
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -664,10 +727,11 @@ tp_status tp_rmsnorm(const tp_model* m, const tp_bf16* x, const tp_bf16* w, int3
   if (!m || M < 0) return TP_ERR_ARG;
   if (M == 0) return TP_OK;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return TP_ERR_ARG;
-  m->stats.kernel_launches++;
-  return cuda_status(launch_rmsnorm(x, m->cfg.hidden, nullptr, w, M, m->cfg.hidden,
-                                    m->cfg.rms_eps, y, m->cfg.hidden,
-                                    static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch(m, "rmsnorm", st, [&] {
+    return launch_rmsnorm(x, m->cfg.hidden, nullptr, w, M, m->cfg.hidden, m->cfg.rms_eps, y,
+                          m->cfg.hidden, st);
+  }));
 }
 
 static tp_status check_batch(const tp_model* m, const tp_batch_t* b) {
@@ -700,8 +764,9 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   if (!kc || !vc || !aligned16(kc) || !aligned16(vc)) return TP_ERR_ARG;
   tp_status s;
   // u = RMSNorm(h)
-  m->stats.kernel_launches++;
-  TP_CHECK_CUDA(launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st));
+  TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
+    return launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st);
+  }));
   // qkv (column-parallel) + RoPE + K/V into the rank caches
   EpiArgs e = base_epi(m, M);
   e.out = q;
@@ -714,7 +779,7 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   e.positions = b->positions;
   e.token_seq = b->token_seq;
   e.rope = m->rope;
-  if ((s = run_column(m, Ls.qkv, u, H, M, EPI_QKV, e, ws, L, st)) != TP_OK) return s;
+  if ((s = run_column(m, "gemm_qkv", Ls.qkv, u, H, M, EPI_QKV, e, ws, L, st)) != TP_OK) return s;
   // attention
   AttnArgs a;
   memset(&a, 0, sizeof(a));
@@ -737,29 +802,30 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   a.l_max = b->l_max;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
   a.status = m->status;
-  m->stats.kernel_launches++;
   if (b->mode == TP_DECODE) {
     a.tiles_per_bg = cdiv(b->max_ctx, 64);
     a.total_units = (int64_t)b->n_seqs * c.n_kv_heads * a.tiles_per_bg;
     a.grid = (int)std::min<int64_t>(m->num_sms, a.total_units);
     a.partials = at<float>(ws, L.attn_partials);
     a.tickets = at<int>(ws, L.attn_tickets);
-    TP_CHECK_CUDA(launch_attn_decode(a, st));
+    TP_CHECK_CUDA(launch(m, "attn_decode", st, [&] { return launch_attn_decode(a, st); }));
   } else {
-    TP_CHECK_CUDA(launch_attn_prefill(a, cdiv(b->max_q_per_seq, 64), st));
+    const int nqb = cdiv(b->max_q_per_seq, 64);
+    TP_CHECK_CUDA(launch(m, "attn_prefill", st, [&] { return launch_attn_prefill(a, nqb, st); }));
   }
   // o_proj (row-parallel) + reduction ① + residual
-  if ((s = run_row(m, Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st)) != TP_OK)
+  if ((s = run_row(m, "gemm_o", Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st)) != TP_OK)
     return s;
   // u = RMSNorm(h); gate_up (column-parallel) + SiLU(gate) * up
-  m->stats.kernel_launches++;
-  TP_CHECK_CUDA(launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st));
+  TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
+    return launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st);
+  }));
   EpiArgs e2 = base_epi(m, M);
   e2.out = act;
   e2.ld_out = c.intermediate;
-  if ((s = run_column(m, Ls.gate_up, u, H, M, EPI_SILU, e2, ws, L, st)) != TP_OK) return s;
+  if ((s = run_column(m, "gemm_gate_up", Ls.gate_up, u, H, M, EPI_SILU, e2, ws, L, st)) != TP_OK) return s;
   // down_proj (row-parallel) + reduction ② + residual
-  return run_row(m, Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws, L, st);
+  return run_row(m, "gemm_down", Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws, L, st);
 }
 
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
@@ -789,14 +855,15 @@ tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
   for (int l = 0; l < m->cfg.n_layers; ++l)
     if ((s = layer_forward(m, l, b, h, fused, ws, L, st)) != TP_OK) return s;
   uint16_t* hs = at<uint16_t>(ws, L.hs);
-  m->stats.kernel_launches++;
-  TP_CHECK_CUDA(launch_rmsnorm(h, m->cfg.hidden, b->sample_rows, m->final_norm, b->n_samples,
-                               m->cfg.hidden, m->cfg.rms_eps, hs, m->cfg.hidden, st));
+  TP_CHECK_CUDA(launch(m, "rmsnorm_final", st, [&] {
+    return launch_rmsnorm(h, m->cfg.hidden, b->sample_rows, m->final_norm, b->n_samples,
+                          m->cfg.hidden, m->cfg.rms_eps, hs, m->cfg.hidden, st);
+  }));
   EpiArgs e = base_epi(m, b->n_samples);
   e.out = logits;
   e.ld_out = ld_logits;
   count_gather(m, b->n_samples);
-  return run_column(m, m->lm, hs, m->cfg.hidden, b->n_samples, EPI_LOGITS, e, ws, L, st);
+  return run_column(m, "gemm_lm_head", m->lm, hs, m->cfg.hidden, b->n_samples, EPI_LOGITS, e, ws, L, st);
 }
 
 tp_status tp_get_stats(const tp_model* m, tp_stats_t* out) {
