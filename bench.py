@@ -241,13 +241,19 @@ def run_ours(args, rank, world):
         dist.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
-    ms, prof, launches = timed_steps(model, batch, h, args.steps, args.warmup, args.rotate,
-                                     args.fused, stream, profile=True)
+    ms, _, launches = timed_steps(model, batch, h, args.steps, args.warmup, args.rotate,
+                                  args.fused, stream, profile=False)
     t_host1 = time.time()
     if world > 1:
         dist.barrier()
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
+    # per-kernel durations: the same steps again with two CUDA events recorded
+    # around every launch on the launch stream (the brackets cost a few
+    # microseconds per launch, so they stay out of the headline region)
+    prof_steps = min(args.steps, 2000)
+    ms_prof, prof, _ = timed_steps(model, batch, h, prof_steps, 0, args.rotate, args.fused,
+                                   stream, profile=True)
     if world > 1:
         tm = torch.tensor([ms], device="cuda")
         dist.all_reduce(tm, op=dist.ReduceOp.MAX)
@@ -365,6 +371,9 @@ def run_ours(args, rank, world):
             "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
             "step_hbm_frac": round(step_gbs / hbm_peak, 3),
             "per_t": per_t, "kernels": kernels,
+            "kernel_timing": f"CUDA events around each launch on the launch stream, {prof_steps} "
+                             f"steps right after the timed region ({ms_prof / prof_steps:.4f} "
+                             "ms/step with the events)",
         },
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -11,17 +11,8 @@ namespace tpk {
 constexpr int kStatusTokenRange = 4;
 constexpr int kStatusTimeout = 7;
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 __device__ __forceinline__ void record_status(int* status, int code) {
@@ -64,16 +55,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
-// (and records a timeout in *status) if that takes longer than kWaitLimitNs.
+// (and records a timeout in *status) once about kWaitLimitCycles SM cycles
+// (~2 s at the GB300 clock) have passed; the cycle counter is read only every
+// 64 failed polls.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  long long t0 = -1;
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
-      record_status(status, kStatusTimeout);
-      return false;
+    if ((++n & 63u) == 0) {
+      const long long now = clock64();
+      if (t0 < 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitCycles) {
+        record_status(status, kStatusTimeout);
+        return false;
+      }
     }
   }
 }
