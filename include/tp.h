@@ -238,6 +238,32 @@ tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
                      tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
                      size_t ws_bytes, void* stream);
 
+/* tp_row_linear_reduce with fused = 1, for callers that cannot allocate
+ * device memory — for example a plug-in that its host framework hands only
+ * input and output tensors, or a latency-critical loop that cannot afford
+ * cudaMalloc's implicit device-wide synchronisation.  The pages have no
+ * counterpart: this is a packaging of the same computation, which it returns
+ * bit for bit as tp_row_linear_reduce (fused) does.
+ *   Arguments: as tp_row_linear_reduce, minus the workspace.
+ *   Scratch: the GEMM's split partials and arrival tickets live in one
+ *     library-owned array in device memory of 10 MiB + 16 KiB (allocated when
+ *     the library is loaded, on every GPU that loads it, held until the
+ *     process exits).  It limits M to 64 tokens and the GPU to 160 SMs; larger
+ *     requests return TP_ERR_WORKSPACE.  The tickets are cleared on `stream`
+ *     before each launch.
+ *   Set-up: the first call on each device resolves the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   Concurrency: every call shares the one array, so calls that may overlap
+ *     on the GPU (different streams, or different host threads) race; order
+ *     them on one stream.
+ *   Allocation: the call makes no cudaMalloc/cudaFree and calls no allocating
+ *     library routine. */
+tp_status tp_row_linear_reduce_noalloc(const tp_model* m, int32_t layer, int32_t which,
+                                       const tp_bf16* x, int64_t x_rank_stride, int64_t ldx,
+                                       int32_t M, const tp_bf16* residual, tp_bf16* y,
+                                       void* stream);
+
 /* Replicated RMSNorm (P1 §3.2: small layers stay whole on every rank):
  * y = x / sqrt(mean(x^2) + eps) * w, fp32 arithmetic, bf16 in and out.
  *   x, y : [M, H] (may alias); w : [H] — any device vector. */

@@ -88,6 +88,8 @@ _SIGS = {
                                    c_void_p, c_size_t, c_void_p]),
     "tp_forward": (c_int32, [c_void_p, c_void_p, POINTER(tp_batch_t), c_void_p, c_void_p, c_int64,
                              c_int32, c_void_p, c_size_t, c_void_p]),
+    "tp_row_linear_reduce_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int64,
+                                               c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
     "tp_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "tp_get_stats": (c_int32, [c_void_p, POINTER(tp_stats_t)]),
     "tp_reset_stats": (None, [c_void_p]),
@@ -172,6 +174,12 @@ def tp_row_linear_reduce(model, layer, which, x, x_rank_stride, ldx, M, residual
                          ws_bytes, stream) -> int:
     return lib().tp_row_linear_reduce(model, layer, which, x, x_rank_stride, ldx, M, residual, y,
                                       fused, ws, ws_bytes, stream)
+
+
+def tp_row_linear_reduce_noalloc(model, layer, which, x, x_rank_stride, ldx, M, residual, y,
+                                 stream) -> int:
+    return lib().tp_row_linear_reduce_noalloc(model, layer, which, x, x_rank_stride, ldx, M,
+                                              residual, y, stream)
 
 
 def tp_vocab_embed(model, ids, M, h, stream) -> int:

@@ -24,7 +24,7 @@ N_EPI = 6
 
 def _units():
     units = []
-    for name in ("small", "attention", "tp_api"):
+    for name in ("small", "attention", "tp_api", "no_alloc"):
         units.append((os.path.join(CSRC, name + ".cu"), os.path.join(BUILD, name + ".o"), []))
     for e in range(N_EPI):
         units.append((os.path.join(CSRC, "gemm_inst.cu"), os.path.join(BUILD, f"gemm_epi{e}.o"),

@@ -887,3 +887,39 @@ tp_status tp_check_device(tp_model* m, void* stream) {
 }
 
 }  // extern "C"
+
+// ============================================================================
+// Fused row-parallel reduction whose stream-K partials and tickets live in a
+// fixed scratch region the caller already owns (the no-allocation entry point
+// in no_alloc.cu passes its static device array).  Layout of the region:
+// [tickets: ticket_bytes][partials: partial_bytes].  The tickets are cleared
+// on `st` before the launch.
+// ============================================================================
+namespace tpk {
+tp_status row_reduce_in_scratch(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
+                                int64_t x_rank_stride, int64_t ldx, int32_t M,
+                                const tp_bf16* residual, tp_bf16* y, void* scratch,
+                                size_t ticket_bytes, size_t partial_bytes, int32_t max_tokens,
+                                cudaStream_t st) {
+  if (!valid_layer(m, layer) || (which != TP_O && which != TP_DOWN) || M < 0 || !scratch)
+    return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  const ShardedLinear& W = which == TP_O ? m->layers[layer].o : m->layers[layer].down;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      x_rank_stride % 8 || ldx % 8 || ldx < W.cols)
+    return TP_ERR_ARG;
+  if (M > max_tokens) return TP_ERR_WORKSPACE;
+  const GemmPlan p = plan_gemm(M);
+  if (!p.swap) return TP_ERR_WORKSPACE;
+  const size_t tiles = (size_t)cdiv(W.rows, 128);
+  const size_t partials = (size_t)m->num_sms * 2 * p.BN * 128 * sizeof(float);
+  if (tiles * sizeof(int) > ticket_bytes || partials > partial_bytes) return TP_ERR_WORKSPACE;
+  TP_CHECK_CUDA(cudaMemsetAsync(scratch, 0, tiles * sizeof(int), st));
+  WsLayout L;
+  memset(&L, 0, sizeof(L));
+  L.gemm_tickets = 0;
+  L.gemm_partials = ticket_bytes;
+  return run_row(m, "gemm_row_noalloc", W, x, x_rank_stride, ldx, M, residual, y, 1, scratch, L,
+                 st);
+}
+}  // namespace tpk
