@@ -199,7 +199,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
     fence_barrier_init();
     fence_proxy_async_smem();
   }
+  if (threadIdx.x == kDecWarps * 32) {  // producer: descriptors are parameters, fetch early
+    tma_prefetch_desc(&a.tmK);
+    tma_prefetch_desc(&a.tmV);
+  }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // q and the cache rows were written by the preceding kernels
 
   const int G = a.grid, c = blockIdx.x;
   const int64_t T = a.total_units;
@@ -209,14 +215,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   if (warp == kDecWarps) {
     // producer
     if (lane == 0) {
-      tma_prefetch_desc(&a.tmK);
-      tma_prefetch_desc(&a.tmV);
       const uint64_t pol = policy_evict_first();
       uint32_t n = 0;
+      // (sequence, KV head, tile) of unit u, walked incrementally
+      const int64_t bg0 = beg / TB;
+      int tile = static_cast<int>(beg - bg0 * TB);
+      int b = static_cast<int>(bg0 / a.n_kv), g = static_cast<int>(bg0 % a.n_kv);
       for (int64_t u = beg; u < end; ++u) {
-        const int64_t bg = u / TB;
-        const int tile = static_cast<int>(u - bg * TB);
-        const int b = static_cast<int>(bg / a.n_kv), g = static_cast<int>(bg % a.n_kv);
+        if (u != beg && ++tile == TB) {
+          tile = 0;
+          if (++g == a.n_kv) { g = 0; ++b; }
+        }
         const int slice = ((g / a.kv_r) * a.n_seqs + b) * a.kv_r + (g % a.kv_r);
         const uint32_t s = n % S, ph = (n / S) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
@@ -421,6 +430,8 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
   int* flags = reinterpret_cast<int*>(full + kPreStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();  // q and the cache were written by the preceding kernels
   const int b = blockIdx.z, h = blockIdx.y;
   const int n_qb = gridDim.x;
   const int qb = n_qb - 1 - blockIdx.x;  // longest blocks first
@@ -536,8 +547,7 @@ static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attn_decode_kernel<D><<<a.grid, kDecThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(attn_decode_kernel<D>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
 }
 
 template <int D>
@@ -551,8 +561,7 @@ static cudaError_t launch_prefill_t(const AttnArgs& a, int n_qb, cudaStream_t st
     attr = true;
   }
   dim3 grid(n_qb, a.n_heads, a.n_seqs);
-  attn_prefill_kernel<D><<<grid, kPreThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(attn_prefill_kernel<D>, grid, dim3(kPreThreads), smem, st, a);
 }
 
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st) {

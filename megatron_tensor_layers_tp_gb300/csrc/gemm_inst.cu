@@ -22,7 +22,7 @@ cudaError_t TPK_CAT(launch_gemm_epi, TPK_EPI)(bool swap, const GemmArgs& a, size
       if (e != cudaSuccess) return e;
       attr_swap = true;
     }
-    gemm_kernel<true, TPK_EPI><<<a.grid, kThreads, smem, st>>>(a);
+    return launch_k(gemm_kernel<true, TPK_EPI>, dim3(a.grid), dim3(kThreads), smem, st, a);
   } else {
     if (!attr_norm) {
       cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false, TPK_EPI>,
@@ -30,7 +30,7 @@ cudaError_t TPK_CAT(launch_gemm_epi, TPK_EPI)(bool swap, const GemmArgs& a, size
       if (e != cudaSuccess) return e;
       attr_norm = true;
     }
-    gemm_kernel<false, TPK_EPI><<<a.grid, kThreads, smem, st>>>(a);
+    return launch_k(gemm_kernel<false, TPK_EPI>, dim3(a.grid), dim3(kThreads), smem, st, a);
   }
   return cudaGetLastError();
 }

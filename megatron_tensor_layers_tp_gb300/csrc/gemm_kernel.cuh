@@ -74,14 +74,21 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
     const int f = arow;
     const bool fval = f < a.a_rows_valid;
     if constexpr (EPI == EPI_RESID) {
+      // The residual is usually the output buffer itself (in-place update of
+      // the hidden state): read all 16 values before the first store so the
+      // loads are not serialised behind stores to the same buffer.
       uint16_t* out = static_cast<uint16_t*>(e.out);
+      float r[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = brow0 + j;
-        if (fval && m < e.M) {
-          float r = e.residual ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f]) : 0.f;
-          out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + r);
-        }
+        r[j] = (e.residual && fval && m < e.M) ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f])
+                                               : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + r[j]);
       }
     } else if constexpr (EPI == EPI_PARTIAL) {
       float* out = static_cast<float*>(e.out) + (int64_t)g * e.out_group_stride;
@@ -129,23 +136,38 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       const bool primary = (g % e.kv_replicas) == 0;
       const int copy = g / e.kv_replicas;
       uint16_t* qout = static_cast<uint16_t*>(e.out);
+      // all loads (positions, sequences, RoPE factors) first, then the stores
+      int pos_[16], seq_[16];
+      float2 cs_[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int m = brow0 + j;
+        const bool ok = fval && m < e.M;
+        pos_[j] = ok ? e.positions[m] : -1;
+        seq_[j] = (ok && kind != 0) ? e.token_seq[m] : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool ok = pos_[j] >= 0 && pos_[j] < e.l_max;
+        cs_[j] = (ok && kind != 2) ? e.rope[(int64_t)pos_[j] * half + jp] : make_float2(1.f, 0.f);
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
         const int m = brow0 + j;
         if (!fval || m >= e.M) continue;
-        const int pos = e.positions[m];
+        const int pos = pos_[j];
         if (pos < 0 || pos >= e.l_max) continue;  // never index the cache or table out of range
         float val = v[j];
         if (kind != 2) {
-          const float2 cs = e.rope[(int64_t)pos * half + jp];
+          const float2 cs = cs_[j];
           val = second ? (v[j] * cs.x + partner * cs.y) : (v[j] * cs.x - partner * cs.y);
         }
         if (kind == 0) {
           qout[(int64_t)m * e.ld_out + (int64_t)(g * e.q_heads_per_rank + head) * d + feat] =
               f_to_bf16(val);
         } else if (primary) {
-          const int seq = e.token_seq[m];
+          const int seq = seq_[j];
           uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
           const int64_t idx = copy * e.kv_copy_stride +
                               (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d + feat;
@@ -324,41 +346,86 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int K = a.k_slices * a.k_iters_slice;  // K steps per tile
   const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
 
+  // Launched with programmatic stream serialisation: the next kernel may start
+  // its own set-up now.  Everything below that reads data written by an
+  // earlier kernel comes after pdl_wait(); only the weight shards (written
+  // once when the model was loaded) are fetched before it.
+  pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
-      uint32_t n = 0;
-      bool ok = true;
-      for (int64_t it = beg; it < end && ok;) {
+      // Load n of this CTA is flat iteration beg + n.  Its operand coordinates
+      // are walked incrementally (integer division only once, at the start).
+      struct Cursor {
+        int g, ia, ib, ks, kk;
+      };
+      auto start_at = [&](int64_t it) {
+        Cursor c;
         const int64_t tile = it / K;
-        const int64_t seg_end = min(end, (tile + 1) * K);
-        const int ia = static_cast<int>(tile % a.a_tiles);
+        const int k = static_cast<int>(it - tile * K);
+        c.ia = static_cast<int>(tile % a.a_tiles);
         const int64_t rest = tile / a.a_tiles;
-        const int ib = static_cast<int>(rest % a.b_tiles);
-        const int g = static_cast<int>(rest / a.b_tiles);
-        for (int k = static_cast<int>(it - tile * K); k < static_cast<int>(seg_end - tile * K); ++k) {
-          const uint32_t s = n % S, ph = (n / S) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1, a.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], kATileBytes + b_tile_bytes);
-          const int ks = k / a.k_iters_slice, kk = k - ks * a.k_iters_slice;
-          const int sa = slice_of(a.a_slice_mode, g, ks), sb = slice_of(a.b_slice_mode, g, ks);
+        c.ib = static_cast<int>(rest % a.b_tiles);
+        c.g = static_cast<int>(rest / a.b_tiles);
+        c.ks = k / a.k_iters_slice;
+        c.kk = k - c.ks * a.k_iters_slice;
+        return c;
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.kk < a.k_iters_slice) return;
+        c.kk = 0;
+        if (++c.ks < a.k_slices) return;
+        c.ks = 0;
+        if (++c.ia < a.a_tiles) return;
+        c.ia = 0;
+        if (++c.ib < a.b_tiles) return;
+        c.ib = 0;
+        ++c.g;
+      };
+      // decode orientation: A holds the weights; prefill orientation: B does
+      auto issue = [&](const Cursor& c, uint32_t s, bool weights) {
+        if (weights == SWAP) {
+          const int sa = slice_of(a.a_slice_mode, c.g, c.ks);
           if (a.a_slice_mid)
-            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, sa, ia * 128, polA);
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], c.kk * 64, sa, c.ia * 128, polA);
           else
-            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, ia * 128, sa, polA);
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], c.kk * 64, c.ia * 128, sa, polA);
+        } else {
+          const int sb = slice_of(a.b_slice_mode, c.g, c.ks);
           if (a.b_slice_mid)
-            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, sb, ib * BN, polB);
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], c.kk * 64, sb, c.ib * BN, polB);
           else
-            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, ib * BN, sb, polB);
-          ++n;
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], c.kk * 64, c.ib * BN, sb, polB);
         }
-        it = seg_end;
+      };
+      const uint32_t pre = static_cast<uint32_t>(end - beg < (int64_t)S ? end - beg : (int64_t)S);
+      Cursor cur = start_at(beg);
+      for (uint32_t n = 0; n < pre; ++n) {  // first use of each stage: nothing to wait for
+        mbar_arrive_expect_tx(&full[n], kATileBytes + b_tile_bytes);
+        issue(cur, n, true);
+        advance(cur);
+      }
+      pdl_wait();
+      cur = start_at(beg);
+      uint32_t n = 0;
+      for (int64_t it = beg; it < end; ++it, ++n) {
+        const uint32_t s = n % S, ph = (n / S) & 1;
+        if (n >= pre) {
+          if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
+          mbar_arrive_expect_tx(&full[s], kATileBytes + b_tile_bytes);
+          issue(cur, s, true);
+        }
+        issue(cur, s, false);
+        advance(cur);
       }
       // never leave with bulk copies still landing in shared memory
       for (uint32_t i = (n > (uint32_t)S ? n - S : 0); i < n; ++i)
         mbar_wait(&full[i % S], (i / S) & 1, a.status);
+    } else {
+      pdl_wait();
     }
   } else if (warp == 1) {
+    pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, BN);
       uint32_t n = 0, seg = 0;
@@ -392,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_wait(drain, 0, a.status);
     }
   } else {
+    pdl_wait();
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     uint32_t seg = 0;
@@ -447,16 +515,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         bar_sync(1, 128);
         if (*last_flag) {
           __threadfence();
+          // the pieces in K order; loads of 4 pieces are issued before their adds
+          const int64_t tile_k0 = tile * K;
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            for (int sgi = 0; sgi < nseg; ++sgi) {
-              const int cc = c_first + sgi;
-              const int slot = (range_begin(cc, T, G) / K == tile) ? 0 : 1;
-              const float* src = a.partials + ((int64_t)(cc * 2 + slot) * BN) * 128;
+            for (int s0 = 0; s0 < nseg; s0 += 4) {
+              float tmp[4][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(&src[(c0 + j) * 128 + row]);
+              for (int q = 0; q < 4; ++q) {
+                const int cc = c_first + s0 + q;
+                if (s0 + q < nseg) {
+                  const int slot = range_begin(cc, T, G) >= tile_k0 ? 0 : 1;
+                  const float* src = a.partials + ((int64_t)(cc * 2 + slot) * BN) * 128;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) tmp[q][j] = __ldcg(&src[(c0 + j) * 128 + row]);
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (s0 + q < nseg) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[j] += tmp[q][j];
+                }
             }
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v);
           }

@@ -89,6 +89,26 @@ struct AttnArgs {
   int* status;
 };
 
+// Every kernel on the forward path is launched with programmatic stream
+// serialisation: it may begin (set-up, weight prefetch) while its predecessor
+// on the stream finishes, and waits (griddepcontrol.wait) before touching data
+// a predecessor wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // gemm.cu / gemm_epi*.cu
 cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st);
 #define TPK_DECLARE_EPI(E) \

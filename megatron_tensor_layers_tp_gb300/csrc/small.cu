@@ -26,6 +26,8 @@ namespace tpk {
 __global__ void embed_kernel(const uint16_t* __restrict__ table, int vocab, int vocab_per_rank,
                              int t, const int32_t* __restrict__ ids, int M, int H,
                              uint16_t* __restrict__ h, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= M) return;
@@ -50,9 +52,8 @@ cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, i
   if (M == 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int blocks = (M + warps_per_block - 1) / warps_per_block;
-  embed_kernel<<<blocks, warps_per_block * 32, 0, st>>>(table, vocab, vocab_per_rank, t, ids, M,
-                                                         H, h, status);
-  return cudaGetLastError();
+  return launch_k(embed_kernel, dim3(blocks), dim3(warps_per_block * 32), 0, st, table, vocab,
+                  vocab_per_rank, t, ids, M, H, h, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ rows,
     const uint16_t* __restrict__ w, int H, float eps, uint16_t* __restrict__ y, int64_t ldy) {
   __shared__ float red[kNormThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();
   const int i = blockIdx.x;
   const int src_row = rows ? rows[i] : i;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)src_row * ldx);
@@ -108,8 +111,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
                            int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(x, ldx, rows, w, H, eps, y, ldy);
-  return cudaGetLastError();
+  return launch_k(rmsnorm_kernel, dim3(M), dim3(kNormThreads), 0, st, x, ldx, rows, w, H, eps, y,
+                  ldy);
 }
 
 // ---------------------------------------------------------------------------
@@ -120,6 +123,8 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, 
 __global__ void reduce_ranks_kernel(const float4* __restrict__ P, int64_t rank_stride4, int t,
                                     int64_t n4, int H4, const uint2* __restrict__ residual,
                                     uint2* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 acc = P[i];
@@ -144,11 +149,9 @@ cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int 
   if (n4 == 0) return cudaSuccess;
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
-  reduce_ranks_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(partials),
-                                              rank_stride / 4, t, n4, H / 4,
-                                              reinterpret_cast<const uint2*>(residual),
-                                              reinterpret_cast<uint2*>(y));
-  return cudaGetLastError();
+  return launch_k(reduce_ranks_kernel, dim3(blocks), dim3(256), 0, st,
+                  reinterpret_cast<const float4*>(partials), rank_stride / 4, t, n4, H / 4,
+                  reinterpret_cast<const uint2*>(residual), reinterpret_cast<uint2*>(y));
 }
 
 // ---------------------------------------------------------------------------
