@@ -60,27 +60,27 @@ __device__ __forceinline__ uint32_t kv_off(int row, int ch) {
 
 constexpr int kKeyTile = 64;
 
-// One warp: scores of 16 query rows against 64 keys, then the online-softmax
-// update of (m, l, O).  qa: Q A-fragments; sK/sV: smem tiles.  key0: position
-// of the first key; lim[2]: last visible key position (inclusive) of the
-// thread's two rows.
-template <int D>
+// One warp: scores of 16 query rows against NKT*8 keys (rows krow0.. of the
+// smem tile), then the online-softmax update of (m, l, O).  qa: Q
+// A-fragments; sK/sV: smem tiles.  key0: position of the first of those keys;
+// lim[2]: last visible key position (inclusive) of the thread's two rows.
+template <int D, int NKT>
 __device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint32_t sK,
-                                          uint32_t sV, int key0, const int (&lim)[2],
+                                          uint32_t sV, int krow0, int key0, const int (&lim)[2],
                                           float scale_log2, float (&m)[2], float (&l)[2],
                                           float (&o)[D / 8][4]) {
   const int lane = threadIdx.x & 31;
-  float s[8][4];
+  float s[NKT][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NKT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-    for (int np = 0; np < 4; ++np) {  // pairs of 8-key n-tiles
+    for (int np = 0; np < NKT / 2; ++np) {  // pairs of 8-key n-tiles
       const int j = lane >> 3, r = lane & 7;
-      const int key = (np * 2 + (j >> 1)) * 8 + r;
+      const int key = krow0 + (np * 2 + (j >> 1)) * 8 + r;
       const int ch = kk * 2 + (j & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(sK + kv_off(key, ch), b0, b1, b2, b3);
@@ -91,7 +91,7 @@ __device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint3
   // mask + tile row max
   float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < NKT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int key = key0 + nt * 8 + (lane & 3) * 2 + (i & 1);
@@ -119,9 +119,9 @@ __device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint3
     o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
     o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
   }
-  uint32_t pa[4][4];
+  uint32_t pa[NKT / 2][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
+  for (int nt = 0; nt < NKT; ++nt) {
     float p[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -134,11 +134,11 @@ __device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint3
   }
   // O += P V
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
+  for (int kk = 0; kk < NKT / 2; ++kk) {
 #pragma unroll
     for (int np = 0; np < D / 16; ++np) {
       const int j = lane >> 3, r = lane & 7;
-      const int key = kk * 16 + (j & 1) * 8 + r;
+      const int key = krow0 + kk * 16 + (j & 1) * 8 + r;
       const int ch = np * 2 + (j >> 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(sV + kv_off(key, ch), b0, b1, b2, b3);
@@ -172,7 +172,7 @@ struct DecSmem {
   static constexpr int kTileBytes = (D / 64) * 8192;       // one K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kQRow = D * 2 + 16;                 // padded bf16 row
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kComb = kDecWarps * 16 * (D + 2);   // floats: O, m, l per warp/row
   static constexpr size_t bytes(int) {
     return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
@@ -195,13 +195,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = L::kStages;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDecWarps); }
     fence_barrier_init();
     fence_proxy_async_smem();
   }
+  uint64_t pol = 0;
   if (threadIdx.x == kDecWarps * 32) {  // producer: descriptors are parameters, fetch early
     tma_prefetch_desc(&a.tmK);
     tma_prefetch_desc(&a.tmV);
+    pol = policy_evict_first();
   }
   __syncthreads();
   pdl_launch_dependents();
@@ -215,7 +217,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   if (warp == kDecWarps) {
     // producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
       uint32_t n = 0;
       // (sequence, KV head, tile) of unit u, walked incrementally
       const int64_t bg0 = beg / TB;
@@ -272,17 +273,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
       const int lim[2] = {pos, pos};
-      for (int i = warp; i < len; i += kDecWarps) {
+      // every warp takes its own 16 keys of every 64-key tile, so a stage is
+      // released after a quarter of the work and the other stages keep
+      // streaming
+      for (int i = 0; i < len; ++i) {
         const uint32_t n = n_base + i;
         const uint32_t s = n % S, ph = (n / S) & 1;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&full[s], ph, a.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { alive = false; break; }
-        const int key0 = (tile0 + i) * kKeyTile;
+        const int key0 = (tile0 + i) * kKeyTile + warp * (kKeyTile / kDecWarps);
         if (key0 <= pos) {
           const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
-          attn_tile<D>(qa, st, st + L::kTileBytes, key0, lim, a.scale_log2, m, l, o);
+          attn_tile<D, kKeyTile / kDecWarps / 8>(qa, st, st + L::kTileBytes,
+                                                 warp * (kKeyTile / kDecWarps), key0, lim,
+                                                 a.scale_log2, m, l, o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
     const int key0 = tile * kKeyTile;
     if (key0 <= warp_max) {
       const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
-      attn_tile<D>(qa, st, st + L::kTileBytes, key0, lim, a.scale_log2, m, l, o);
+      attn_tile<D, 8>(qa, st, st + L::kTileBytes, 0, key0, lim, a.scale_log2, m, l, o);
     }
     __syncthreads();
     if (threadIdx.x == 0 && tile + kPreStages < n_tiles) issue(tile + kPreStages);

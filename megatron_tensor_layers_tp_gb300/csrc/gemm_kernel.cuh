@@ -66,9 +66,50 @@ __device__ __forceinline__ int plain_col(const EpiArgs& e, int f) {
   return base + ((w & 1) ? (w >> 1) + d / 2 : (w >> 1));
 }
 
+// Global inputs of the decode-orientation epilogues (residual values; token
+// positions, sequences and RoPE factors), fetched by epi_load ahead of the
+// arithmetic so their latency overlaps the other loads of a fix-up.
+struct EpiIn {
+  float r[16];
+  int pos[16];
+  int seq[16];
+  float2 cs[16];
+};
+
+template <bool SWAP, int EPI>
+__device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int brow0, EpiIn& in) {
+  const EpiArgs& e = a.e;
+  const int f = arow;
+  const bool fval = f < a.a_rows_valid;
+  if constexpr (SWAP && EPI == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = brow0 + j;
+      in.r[j] = (e.residual && fval && m < e.M) ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f])
+                                                : 0.f;
+    }
+  } else if constexpr (SWAP && EPI == EPI_QKV) {
+    int kind = 2, head = 0, w = 0;
+    if (fval) qkv_classify(e, f, kind, head, w);
+    const int half = e.head_dim / 2, jp = w >> 1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = brow0 + j;
+      const bool ok = fval && m < e.M;
+      in.pos[j] = ok ? e.positions[m] : -1;
+      in.seq[j] = (ok && kind != 0) ? e.token_seq[m] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const bool ok = in.pos[j] >= 0 && in.pos[j] < e.l_max;
+      in.cs[j] = (ok && kind != 2) ? e.rope[(int64_t)in.pos[j] * half + jp] : make_float2(1.f, 0.f);
+    }
+  }
+}
+
 template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
-                                          float (&v)[16]) {
+                                          float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
   if constexpr (SWAP) {
     const int f = arow;
@@ -78,17 +119,10 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       // the hidden state): read all 16 values before the first store so the
       // loads are not serialised behind stores to the same buffer.
       uint16_t* out = static_cast<uint16_t*>(e.out);
-      float r[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int m = brow0 + j;
-        r[j] = (e.residual && fval && m < e.M) ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f])
-                                               : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = brow0 + j;
-        if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + r[j]);
+        if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + in.r[j]);
       }
     } else if constexpr (EPI == EPI_PARTIAL) {
       float* out = static_cast<float*>(e.out) + (int64_t)g * e.out_group_stride;
@@ -136,38 +170,23 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       const bool primary = (g % e.kv_replicas) == 0;
       const int copy = g / e.kv_replicas;
       uint16_t* qout = static_cast<uint16_t*>(e.out);
-      // all loads (positions, sequences, RoPE factors) first, then the stores
-      int pos_[16], seq_[16];
-      float2 cs_[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int m = brow0 + j;
-        const bool ok = fval && m < e.M;
-        pos_[j] = ok ? e.positions[m] : -1;
-        seq_[j] = (ok && kind != 0) ? e.token_seq[m] : 0;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const bool ok = pos_[j] >= 0 && pos_[j] < e.l_max;
-        cs_[j] = (ok && kind != 2) ? e.rope[(int64_t)pos_[j] * half + jp] : make_float2(1.f, 0.f);
-      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
         const int m = brow0 + j;
         if (!fval || m >= e.M) continue;
-        const int pos = pos_[j];
+        const int pos = in.pos[j];
         if (pos < 0 || pos >= e.l_max) continue;  // never index the cache or table out of range
         float val = v[j];
         if (kind != 2) {
-          const float2 cs = cs_[j];
+          const float2 cs = in.cs[j];
           val = second ? (v[j] * cs.x + partner * cs.y) : (v[j] * cs.x - partner * cs.y);
         }
         if (kind == 0) {
           qout[(int64_t)m * e.ld_out + (int64_t)(g * e.q_heads_per_rank + head) * d + feat] =
               f_to_bf16(val);
         } else if (primary) {
-          const int seq = seq_[j];
+          const int seq = in.seq[j];
           uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
           const int64_t idx = copy * e.kv_copy_stride +
                               (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d + feat;
@@ -485,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (nseg == 1) {
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
+          EpiIn in;
+          epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
           tmem_ld16(taddr + c0, v);
           tmem_ld_wait();
-          epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v);
+          epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
         }
         tc_fence_before();
         __syncwarp();
@@ -518,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           // the pieces in K order; loads of 4 pieces are issued before their adds
           const int64_t tile_k0 = tile * K;
           for (int c0 = 0; c0 < BN; c0 += 16) {
+            EpiIn in;
+            epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -540,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                   for (int j = 0; j < 16; ++j) v[j] += tmp[q][j];
                 }
             }
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v);
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
           }
           if (threadIdx.x == 64) a.tickets[tile] = 0;
         }

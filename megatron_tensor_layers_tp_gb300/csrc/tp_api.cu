@@ -805,7 +805,20 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   if (b->mode == TP_DECODE) {
     a.tiles_per_bg = cdiv(b->max_ctx, 64);
     a.total_units = (int64_t)b->n_seqs * c.n_kv_heads * a.tiles_per_bg;
-    a.grid = (int)std::min<int64_t>(m->num_sms, a.total_units);
+    // Whole (sequence, KV head) pairs per CTA when they can be dealt out
+    // evenly to at least 80% of the SMs: no pair is then split and no partial
+    // result needs combining.  Otherwise split the flat range evenly.
+    const int64_t n_bg = (int64_t)b->n_seqs * c.n_kv_heads;
+    int grid = (int)std::min<int64_t>(m->num_sms, a.total_units);
+    for (int64_t d = 1; d <= n_bg; ++d) {
+      if (n_bg % d) continue;
+      const int64_t g = n_bg / d;
+      if (g <= m->num_sms) {
+        if (g * 5 >= (int64_t)m->num_sms * 4) grid = (int)g;
+        break;
+      }
+    }
+    a.grid = grid;
     a.partials = at<float>(ws, L.attn_partials);
     a.tickets = at<int>(ws, L.attn_tickets);
     TP_CHECK_CUDA(launch(m, "attn_decode", st, [&] { return launch_attn_decode(a, st); }));
