@@ -47,6 +47,7 @@ def parse():
     p.add_argument("--fused", type=int, default=1)
     p.add_argument("--per-t", type=int, default=1)
     p.add_argument("--cpu-baseline", type=int, default=1)
+    p.add_argument("--prefill", type=int, default=1)
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     return p.parse_args()
@@ -350,6 +351,11 @@ def run_ours(args, rank, world):
     cpu = None
     if args.cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, args.t, args.cpu_budget_s)
+    prefill = None
+    if args.prefill and rank == 0 and world == 1:
+        model.close()
+        torch.cuda.empty_cache()
+        prefill = prefill_section(stream)
 
     model.close()
     if rank != 0:
@@ -370,7 +376,7 @@ def run_ours(args, rank, world):
                   f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
             "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
             "step_hbm_frac": round(step_gbs / hbm_peak, 3),
-            "per_t": per_t, "kernels": kernels,
+            "per_t": per_t, "kernels": kernels, "prefill": prefill,
             "kernel_timing": f"CUDA events around each launch on the launch stream, {prof_steps} "
                              f"steps right after the timed region ({ms_prof / prof_steps:.4f} "
                              "ms/step with the events)",
@@ -382,6 +388,103 @@ def run_ours(args, rank, world):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def prefill_section(stream, reps=10):
+    """Llama-3.1-8B-shaped prefill chunk at t = 4: 8 sequences x 256 tokens
+    through the vocab-parallel embedding, one decoder layer and the
+    vocab-parallel LM head on each sequence's last token.  Reports every
+    kernel's duration and, for the contractions, TFLOP/s against the sustained
+    bf16 tensor-core peak (the GEMMs run inside a multi-kernel step)."""
+    import torch
+    import synth
+    from megatron_tensor_layers_tp_gb300 import binding as B
+    from megatron_tensor_layers_tp_gb300.runtime import TPModel, make_config, prefill_batch
+    w = synth.WORKLOADS["llama8b_prefill"]
+    t = 4
+    H, d, I, V, M = w.hidden, w.head_dim, w.intermediate, w.vocab, w.tokens
+    with torch.cuda.stream(stream):
+        shapes = synth.weight_shapes(w, 0)
+        L = {}
+        for k in LAYER_KINDS:
+            x = torch.empty(shapes[k], dtype=torch.bfloat16, device="cuda")
+            if k.endswith("norm"):
+                x.fill_(1.0)
+            else:
+                synth.fill_normal_(x, w.seed, synth.tensor_id(k, 0), w.sigma_w)
+            L[k] = x
+        emb = torch.empty((V, H), dtype=torch.bfloat16, device="cuda")
+        synth.fill_normal_(emb, w.seed, synth.tensor_id("embed"), w.sigma_w)
+        lm = torch.empty((V, H), dtype=torch.bfloat16, device="cuda")
+        synth.fill_normal_(lm, w.seed, synth.tensor_id("lm_head"), w.sigma_w)
+        fn = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+        cfg = make_config(H, w.n_heads, w.n_kv_heads, d, I, V, 1, t, w.rms_eps, w.rope_theta,
+                          max_positions=w.l_max)
+        model = TPModel(cfg, [L], emb, fn, lm, max_tokens=M, stream=stream)
+        del L, emb, lm
+        k = model.alloc_kv(w.n_seqs, w.l_max)
+        v = model.alloc_kv(w.n_seqs, w.l_max)
+        batch = prefill_batch(w.n_seqs, w.seq_len, [k], [v], w.l_max)
+        ids = torch.empty(M, dtype=torch.int32, device="cuda")
+        synth.fill_uniform_(ids, w.seed, synth.tensor_id("ids"), V)
+        hbuf = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+        logits = torch.empty((w.n_seqs, V), dtype=torch.bfloat16, device="cuda")
+        cb = batch.to_c()
+    torch.cuda.synchronize()
+
+    def run(n):
+        for _ in range(n):
+            model.forward(ids, batch, stream=stream, h=hbuf, logits=logits, cbatch=cb)
+    run(3)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(reps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    B.tp_profile(model.handle, True)
+    run(reps)
+    B.tp_profile(model.handle, False)
+    prof = B.tp_profile_read(model.handle, stream.cuda_stream)
+    assert model.check_device(stream) == 0
+    _, tc_peak, _ = read_peaks()
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    sustained = tc_peak
+    if os.path.exists(pk_path):
+        sustained = json.load(open(pk_path)).get("bf16_tflops_sustained", tc_peak)
+    attn_flops = 0
+    for _ in range(w.n_seqs):
+        attn_flops += 4 * w.n_heads * d * (w.seq_len * (w.seq_len + 1) // 2)
+    flops = {
+        "gemm_qkv": 2 * M * H * (w.n_heads + 2 * w.n_kv_heads) * d,
+        "gemm_o": 2 * M * w.n_heads * d * H,
+        "gemm_gate_up": 2 * M * H * 2 * I,
+        "gemm_down": 2 * M * I * H,
+        "attn_prefill": attn_flops,
+    }
+    kern = {}
+    for name, (n, tot) in prof.items():
+        avg_ms = tot / n
+        e = {"launches": n, "avg_us": round(avg_ms * 1e3, 2)}
+        if name in flops:
+            tf = flops[name] / (avg_ms * 1e-3) / 1e12
+            e["tflops"] = round(tf, 1)
+            e["frac_tc_sustained"] = round(tf / sustained, 3)
+        if name == "gemm_lm_head":
+            gbs = (V * H * 2) / (avg_ms * 1e-3) / 1e9
+            e["gbs"] = round(gbs, 1)
+        kern[name] = e
+    gem = [k for k in ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down") if k in prof]
+    g_flops = sum(flops[k] for k in gem)
+    g_ms = sum(prof[k][1] / prof[k][0] for k in gem)
+    model.close()
+    return {"workload": "8 sequences x 256 tokens, t=4: embedding + 1 layer + LM head on the last "
+                        "token of each sequence", "ms_per_forward": round(ms, 4),
+            "tokens_per_s": round(M / (ms * 1e-3), 1),
+            "gemm_tflops": round(g_flops / (g_ms * 1e-3) / 1e12, 1),
+            "gemm_frac_tc_sustained": round(g_flops / (g_ms * 1e-3) / 1e12 / sustained, 3),
+            "tc_peak_sustained": sustained, "kernels": kern}
 
 
 # ---------------------------------------------------------------------------

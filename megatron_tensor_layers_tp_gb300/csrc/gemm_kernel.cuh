@@ -104,6 +104,29 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
       const bool ok = in.pos[j] >= 0 && in.pos[j] < e.l_max;
       in.cs[j] = (ok && kind != 2) ? e.rope[(int64_t)in.pos[j] * half + jp] : make_float2(1.f, 0.f);
     }
+  } else if constexpr (!SWAP && EPI == EPI_RESID) {
+    // prefill orientation: lane = token m, 16 consecutive features f0..f0+15
+    const int m = arow, f0 = brow0;
+    if (e.residual && m < e.M && f0 < a.b_rows_valid) {
+      const uint4* rp = reinterpret_cast<const uint4*>(e.residual + (int64_t)m * e.ld_res + f0);
+      const uint4 r0 = rp[0], r1 = rp[1];
+      const uint16_t* rb0 = reinterpret_cast<const uint16_t*>(&r0);
+      const uint16_t* rb1 = reinterpret_cast<const uint16_t*>(&r1);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { in.r[j] = bf16_to_f(rb0[j]); in.r[8 + j] = bf16_to_f(rb1[j]); }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) in.r[j] = 0.f;
+    }
+  } else if constexpr (!SWAP && EPI == EPI_QKV) {
+    const int m = arow, f0 = brow0;
+    in.pos[0] = (m < e.M && f0 < a.b_rows_valid) ? e.positions[m] : -1;
+    int kind, head, w;
+    qkv_classify(e, f0, kind, head, w);
+    const bool ok = in.pos[0] >= 0 && in.pos[0] < e.l_max && kind != 2;
+    const float2* cs = e.rope + (int64_t)(ok ? in.pos[0] : 0) * (e.head_dim / 2) + (w >> 1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) in.cs[j] = ok ? cs[j] : make_float2(1.f, 0.f);
   }
 }
 
@@ -200,18 +223,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
     if (m >= e.M || f0 >= a.b_rows_valid) return;
     if constexpr (EPI == EPI_RESID) {
       uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out + f0;
-      float r[16];
-      if (e.residual) {
-        const uint4* rp = reinterpret_cast<const uint4*>(e.residual + (int64_t)m * e.ld_res + f0);
-        uint4 r0 = rp[0], r1 = rp[1];
-        const uint16_t* rb0 = reinterpret_cast<const uint16_t*>(&r0);
-        const uint16_t* rb1 = reinterpret_cast<const uint16_t*>(&r1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { r[j] = bf16_to_f(rb0[j]); r[8 + j] = bf16_to_f(rb1[j]); }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = 0.f;
-      }
+      const float* r = in.r;
       uint4 o0, o1;
       uint32_t* p0 = reinterpret_cast<uint32_t*>(&o0);
       uint32_t* p1 = reinterpret_cast<uint32_t*>(&o1);
@@ -283,17 +295,16 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       int kind, head, w;
       qkv_classify(e, f0, kind, head, w);
       const int d = e.head_dim, half = d / 2;
-      const int pos = e.positions[m];
+      const int pos = in.pos[0];
       if (pos < 0 || pos >= e.l_max) return;  // never index the cache or table out of range
       float outv[16];
       if (kind == 2) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) outv[j] = v[j];
       } else {
-        const float2* cs = e.rope + (int64_t)pos * half + (w >> 1);
-#pragma unroll
+  #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float2 c = cs[j];
+          const float2 c = in.cs[j];
           const float x1 = v[2 * j], x2 = v[2 * j + 1];
           outv[j] = x1 * c.x - x2 * c.y;       // feature jp
           outv[8 + j] = x2 * c.x + x1 * c.y;   // feature jp + d/2
@@ -328,6 +339,43 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
 }
 
 // --------------------------------------------------------------------------
+// Work of CTA c: first W data-parallel waves — tile c + w*G over its whole K
+// range, so all CTAs walk K in lockstep and the operand slices in flight are
+// shared through L2 — then an even share of the flat (tile, K step) range of
+// the remaining tiles (stream-K).  A tile split there is finished by the last
+// CTA to deliver a piece.  Index arithmetic happens once per segment.
+struct Segment {
+  int64_t tile;   // global tile index
+  int k0, k1;     // K steps [k0, k1) of the tile
+  bool sk;        // from the stream-K part (may still be the whole tile)
+};
+
+struct SegIter {
+  int G, c, K, W;
+  int64_t dp_tiles, T, beg, end;
+  int w;
+  int64_t it;
+  __device__ __forceinline__ bool next(Segment& s) {
+    if (w < W) {
+      s.tile = c + (int64_t)w * G;
+      s.k0 = 0;
+      s.k1 = K;
+      s.sk = false;
+      ++w;
+      return true;
+    }
+    if (it >= end) return false;
+    const int64_t ts = it / K;
+    const int64_t seg_end = min(end, (ts + 1) * K);
+    s.tile = dp_tiles + ts;
+    s.k0 = static_cast<int>(it - ts * K);
+    s.k1 = static_cast<int>(seg_end - ts * K);
+    s.sk = true;
+    it = seg_end;
+    return true;
+  }
+};
+
 template <bool SWAP, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -361,9 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t tmem = *tmem_slot;
 
   const int G = a.grid, c = blockIdx.x;
-  const int64_t T = a.total_iters;
+  const int64_t T = a.total_iters;  // stream-K iterations
   const int K = a.k_slices * a.k_iters_slice;  // K steps per tile
+  const int64_t dp_tiles = (int64_t)a.dp_waves * G;
   const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
+  auto make_iter = [&]() {
+    SegIter si;
+    si.G = G; si.c = c; si.K = K; si.W = a.dp_waves;
+    si.dp_tiles = dp_tiles; si.T = T; si.beg = beg; si.end = end;
+    si.w = 0; si.it = beg;
+    return si;
+  };
+  auto tile_coords = [&](int64_t tile, int& g, int& ia, int& ib) {
+    ia = static_cast<int>(tile % a.a_tiles);
+    const int64_t rest = tile / a.a_tiles;
+    ib = static_cast<int>(rest % a.b_tiles);
+    g = static_cast<int>(rest / a.b_tiles);
+  };
 
   // Launched with programmatic stream serialisation: the next kernel may start
   // its own set-up now.  Everything below that reads data written by an
@@ -373,69 +435,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
-      // Load n of this CTA is flat iteration beg + n.  Its operand coordinates
-      // are walked incrementally (integer division only once, at the start).
-      struct Cursor {
-        int g, ia, ib, ks, kk;
-      };
-      auto start_at = [&](int64_t it) {
-        Cursor c;
-        const int64_t tile = it / K;
-        const int k = static_cast<int>(it - tile * K);
-        c.ia = static_cast<int>(tile % a.a_tiles);
-        const int64_t rest = tile / a.a_tiles;
-        c.ib = static_cast<int>(rest % a.b_tiles);
-        c.g = static_cast<int>(rest / a.b_tiles);
-        c.ks = k / a.k_iters_slice;
-        c.kk = k - c.ks * a.k_iters_slice;
-        return c;
-      };
-      auto advance = [&](Cursor& c) {
-        if (++c.kk < a.k_iters_slice) return;
-        c.kk = 0;
-        if (++c.ks < a.k_slices) return;
-        c.ks = 0;
-        if (++c.ia < a.a_tiles) return;
-        c.ia = 0;
-        if (++c.ib < a.b_tiles) return;
-        c.ib = 0;
-        ++c.g;
-      };
-      // decode orientation: A holds the weights; prefill orientation: B does
-      auto issue = [&](const Cursor& c, uint32_t s, bool weights) {
+      // decode orientation: A holds the weights; prefill orientation: B does.
+      // (ks, kk): rank slice and 64-wide step inside it, kept as counters.
+      auto issue = [&](int g, int ia, int ib, int ks, int kk, uint32_t s, bool weights) {
         if (weights == SWAP) {
-          const int sa = slice_of(a.a_slice_mode, c.g, c.ks);
+          const int sa = slice_of(a.a_slice_mode, g, ks);
           if (a.a_slice_mid)
-            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], c.kk * 64, sa, c.ia * 128, polA);
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, sa, ia * 128, polA);
           else
-            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], c.kk * 64, c.ia * 128, sa, polA);
+            tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, ia * 128, sa, polA);
         } else {
-          const int sb = slice_of(a.b_slice_mode, c.g, c.ks);
+          const int sb = slice_of(a.b_slice_mode, g, ks);
           if (a.b_slice_mid)
-            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], c.kk * 64, sb, c.ib * BN, polB);
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, sb, ib * BN, polB);
           else
-            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], c.kk * 64, c.ib * BN, sb, polB);
+            tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, ib * BN, sb, polB);
         }
       };
-      const uint32_t pre = static_cast<uint32_t>(end - beg < (int64_t)S ? end - beg : (int64_t)S);
-      Cursor cur = start_at(beg);
-      for (uint32_t n = 0; n < pre; ++n) {  // first use of each stage: nothing to wait for
-        mbar_arrive_expect_tx(&full[n], kATileBytes + b_tile_bytes);
-        issue(cur, n, true);
-        advance(cur);
+      // first use of each stage needs no wait: put the weight tiles of the
+      // first S loads in flight before waiting for the previous kernel
+      const int kis = a.k_iters_slice;
+      uint32_t pre = 0;
+      {
+        SegIter si = make_iter();
+        Segment sg;
+        while (pre < (uint32_t)S && si.next(sg)) {
+          int g, ia, ib;
+          tile_coords(sg.tile, g, ia, ib);
+          int ks = sg.k0 / kis, kk = sg.k0 - ks * kis;
+          for (int k = sg.k0; k < sg.k1 && pre < (uint32_t)S; ++k, ++pre) {
+            mbar_arrive_expect_tx(&full[pre], kATileBytes + b_tile_bytes);
+            issue(g, ia, ib, ks, kk, pre, true);
+            if (++kk == kis) { kk = 0; ++ks; }
+          }
+        }
       }
       pdl_wait();
-      cur = start_at(beg);
-      uint32_t n = 0;
-      for (int64_t it = beg; it < end; ++it, ++n) {
-        const uint32_t s = n % S, ph = (n / S) & 1;
-        if (n >= pre) {
-          if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
-          mbar_arrive_expect_tx(&full[s], kATileBytes + b_tile_bytes);
-          issue(cur, s, true);
+      uint32_t n = 0, s = 0, ph = 0;  // load count, stage, stage phase
+      bool ok = true;
+      SegIter si = make_iter();
+      Segment sg;
+      while (ok && si.next(sg)) {
+        int g, ia, ib;
+        tile_coords(sg.tile, g, ia, ib);
+        int ks = sg.k0 / kis, kk = sg.k0 - ks * kis;
+        for (int k = sg.k0; k < sg.k1; ++k, ++n) {
+          if (n >= pre) {
+            if (!mbar_wait(&empty[s], ph ^ 1, a.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[s], kATileBytes + b_tile_bytes);
+            issue(g, ia, ib, ks, kk, s, true);
+          }
+          issue(g, ia, ib, ks, kk, s, false);
+          if (++kk == kis) { kk = 0; ++ks; }
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
         }
-        issue(cur, s, false);
-        advance(cur);
       }
       // never leave with bulk copies still landing in shared memory
       for (uint32_t i = (n > (uint32_t)S ? n - S : 0); i < n; ++i)
@@ -447,32 +500,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, BN);
-      uint32_t n = 0, seg = 0;
+      uint32_t seg = 0, s = 0, ph = 0;  // segment count, stage, stage phase
       bool ok = true;
-      for (int64_t it = beg; it < end && ok;) {
-        const int64_t tile = it / K;
-        const int64_t seg_end = min(end, (tile + 1) * K);
+      SegIter si = make_iter();
+      Segment sg;
+      while (ok && si.next(sg)) {
         const uint32_t buf = seg & 1, use = seg >> 1;
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, a.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + buf * BN;
-        const int k0 = static_cast<int>(it - tile * K), k1 = static_cast<int>(seg_end - tile * K);
-        for (int k = k0; k < k1; ++k) {
-          const uint32_t s = n % S, ph = (n / S) & 1;
+        for (int k = sg.k0; k < sg.k1; ++k) {
           if (!mbar_wait(&full[s], ph, a.status)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = smem_desc_sw128(sA + s * kATileBytes);
           const uint64_t db = smem_desc_sw128(sB + s * b_tile_bytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (k > k0 || kk > 0) ? 1u : 0u);
+            tc_mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (k > sg.k0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
-          ++n;
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1; }
         }
         if (!ok) break;
         tc_commit(&acc_full[buf]);
         ++seg;
-        it = seg_end;
       }
       tc_commit(drain);
       mbar_wait(drain, 0, a.status);
@@ -482,13 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     uint32_t seg = 0;
-    for (int64_t it = beg; it < end;) {
-      const int64_t tile = it / K;
-      const int64_t seg_end = min(end, (tile + 1) * K);
-      const int ia = static_cast<int>(tile % a.a_tiles);
-      const int64_t rest = tile / a.a_tiles;
-      const int ib = static_cast<int>(rest % a.b_tiles);
-      const int g = static_cast<int>(rest / a.b_tiles);
+    SegIter si = make_iter();
+    Segment sg;
+    while (si.next(sg)) {
+      int g, ia, ib;
+      tile_coords(sg.tile, g, ia, ib);
       const uint32_t buf = seg & 1, use = seg >> 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&acc_full[buf], use & 1, a.status);
@@ -498,24 +546,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
       const int arow = ia * 128 + row;
       const int brow = ib * BN;
-      const int c_first = owner_of(tile * K, T, G);
-      const int c_last = owner_of((tile + 1) * K - 1, T, G);
-      const int nseg = c_last - c_first + 1;
+      // pieces of this tile in the stream-K part (1 for a data-parallel tile)
+      int nseg = 1, c_first = c;
+      int64_t ts = 0;
+      if (sg.sk) {
+        ts = sg.tile - dp_tiles;
+        c_first = owner_of(ts * K, T, G);
+        nseg = owner_of((ts + 1) * K - 1, T, G) - c_first + 1;
+      }
       if (nseg == 1) {
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float v[16];
-          EpiIn in;
-          epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
-          epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+        if constexpr (SWAP) {
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+            EpiIn in;
+            epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+            tmem_ld16(taddr + c0, v);
+            tmem_ld_wait();
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+          }
+        } else {
+          // inputs of chunk c0 + 16 are fetched before chunk c0 is stored
+          EpiIn cur, nxt;
+          epi_load<SWAP, EPI>(a, g, arow, brow, cur);
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, nxt);
+            float v[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_ld_wait();
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, cur);
+            cur = nxt;
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
       } else {
         // my piece of the tile -> workspace slot 0 (tile where my range starts) or 1
-        const int my_slot = (beg / K == tile) ? 0 : 1;
+        const int my_slot = (beg / K == ts) ? 0 : 1;
         float* mine = a.partials + ((int64_t)(c * 2 + my_slot) * BN) * 128;
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
@@ -530,14 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         __threadfence();
         bar_sync(1, 128);
         if (threadIdx.x == 64) {
-          const int old = atomicAdd(&a.tickets[tile], 1);
+          const int old = atomicAdd(&a.tickets[sg.tile], 1);
           *last_flag = (old == nseg - 1) ? 1 : 0;
         }
         bar_sync(1, 128);
         if (*last_flag) {
           __threadfence();
           // the pieces in K order; loads of 4 pieces are issued before their adds
-          const int64_t tile_k0 = tile * K;
+          const int64_t tile_k0 = ts * K;
           for (int c0 = 0; c0 < BN; c0 += 16) {
             EpiIn in;
             epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
@@ -565,12 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
           }
-          if (threadIdx.x == 64) a.tickets[tile] = 0;
+          if (threadIdx.x == 64) a.tickets[sg.tile] = 0;
         }
         bar_sync(1, 128);
       }
       ++seg;
-      it = seg_end;
     }
   }
 

@@ -61,7 +61,8 @@ struct GemmArgs {
   int a_policy, b_policy;   // L2 policy: 0 normal, 1 evict_first, 2 evict_last
   int a_slice_mid, b_slice_mid;  // 1: tensor map dims are (K, slice, rows)
   int grid;                 // G
-  int64_t total_iters;      // n_tiles * k_slices * k_iters_slice
+  int dp_waves;             // W: tiles [0, W*G) are whole-tile, data-parallel
+  int64_t total_iters;      // (n_tiles - W*G) * k_slices * k_iters_slice (stream-K part)
   float* partials;          // [G][2][BN][128]
   int* tickets;             // [n_tiles], zero on entry and exit
   int* status;              // device status word

@@ -168,6 +168,25 @@ GemmPlan plan_gemm(int M) {
   return p;
 }
 
+// Decode orientation: the flat (tile, K step) range is split evenly over the
+// grid (stream-K): the weights are read once whatever the split.  Prefill
+// orientation: whole tiles in data-parallel waves (all CTAs walk K together,
+// so operand slices are shared through L2), and only the tiles of the last
+// partial wave are split stream-K.
+void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms) {
+  const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
+  const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
+  if (p.swap || n_tiles < num_sms) {
+    a.dp_waves = 0;
+    a.total_iters = n_tiles * K;
+    a.grid = (int)std::min<int64_t>(num_sms, a.total_iters);
+  } else {
+    a.grid = num_sms;
+    a.dp_waves = (int)(n_tiles / num_sms);
+    a.total_iters = (n_tiles - (int64_t)a.dp_waves * num_sms) * K;
+  }
+}
+
 // Workspace regions (all offsets 256-byte aligned).
 struct WsLayout {
   size_t gemm_tickets, attn_tickets, gemm_partials, attn_partials, u, q, o, act, hs, rank_partials,
@@ -276,8 +295,7 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
   a.n_groups = c.t;
   a.k_slices = 1;
   a.k_iters_slice = cdiv(K, 64);
-  a.total_iters = (int64_t)a.n_groups * a.a_tiles * a.b_tiles * a.k_iters_slice;
-  a.grid = (int)std::min<int64_t>(m->num_sms, a.total_iters);
+  set_schedule(a, p, m->num_sms);
   a.partials = at<float>(ws, L.gemm_partials);
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
@@ -347,8 +365,7 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
     a.e.out_group_stride = (int64_t)M * H;
     epi = EPI_PARTIAL;
   }
-  a.total_iters = (int64_t)a.n_groups * a.a_tiles * a.b_tiles * a.k_slices * a.k_iters_slice;
-  a.grid = (int)std::min<int64_t>(m->num_sms, a.total_iters);
+  set_schedule(a, p, m->num_sms);
   TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
   if (!fused) {
     TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {

@@ -207,3 +207,26 @@ def test_zero_tokens_are_a_no_op():
     assert B.tp_column_linear(m.handle, 0, B.TP_QKV, x.data_ptr(), 16, y.data_ptr(), 16 * m.qkv_rows(),
                               ws, 16, 0) == B.STATUS["TP_ERR_WORKSPACE"]
     m.close()
+
+
+@pytest.mark.parametrize("M,inter,t", [(1024, 2432, 1), (2048, 2432, 1), (1100, 1536, 2)])
+def test_prefill_orientation_schedules_match_oracle(M, inter, t):
+    # M=1024, I=2432, t=1: 8 x 19 = 152 gate_up tiles = one whole data-parallel
+    # wave on 152 SMs (empty stream-K part); M=2048: two waves; M=1100: a
+    # ragged last token tile and a stream-K remainder
+    w = _wl(hidden=512, n_heads=8, n_kv=2, head_dim=64, inter=inter)
+    m, _, _ = _model(w, t, head=False)
+    x = _x(M, w.hidden, seed=41)
+    W = oracle_layer(w, 0)
+    p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)
+    xf = to_f64(x)
+    y = m.column_linear(0, B.TP_GATE_UP, x)
+    for r, sh in enumerate(O.shard_gate_up(W, p)):
+        assert rel_err(to_f64(y[r]), O.linear(xf, sh)) <= TOL
+    a = _x(M, inter, seed=42)
+    res = _x(M, w.hidden, seed=43)
+    out = m.row_linear_reduce(0, B.TP_DOWN, a, residual=res, fused=True)
+    ref = O.round_bf16(to_f64(res) + O.linear(to_f64(a), W.wd))
+    assert rel_err(to_f64(out), ref) <= TOL
+    assert m.check_device() == 0
+    m.close()
