@@ -355,7 +355,19 @@ struct SegIter {
   int64_t dp_tiles, T, beg, end;
   int w;
   int64_t it;
+  int split;   // cluster split-K: one segment, 1/split of tile c / split's K range
+  bool used;
   __device__ __forceinline__ bool next(Segment& s) {
+    if (split > 1) {
+      if (used) return false;
+      used = true;
+      const int r = c % split;
+      s.tile = c / split;
+      s.k0 = r * K / split;
+      s.k1 = (r + 1) * K / split;
+      s.sk = false;
+      return true;
+    }
     if (w < W) {
       s.tile = c + (int64_t)w * G;
       s.k0 = 0;
@@ -418,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     si.G = G; si.c = c; si.K = K; si.W = a.dp_waves;
     si.dp_tiles = dp_tiles; si.T = T; si.beg = beg; si.end = end;
     si.w = 0; si.it = beg;
+    si.split = a.cluster_split; si.used = false;
     return si;
   };
   auto tile_coords = [&](int64_t tile, int& g, int& ia, int& ib) {
@@ -426,6 +439,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     ib = static_cast<int>(rest % a.b_tiles);
     g = static_cast<int>(rest / a.b_tiles);
   };
+
+  // Epilogue inputs of this CTA's last segment: that segment's epilogue (or
+  // fix-up) ends the kernel, so in the decode orientation (one 16-column
+  // chunk) its global inputs are fetched as soon as the epilogue warps may
+  // read them, long before the accumulator is ready.
+  EpiIn pre;
+  bool pre_ok = false;
+  int n_segs = 0;
 
   // Launched with programmatic stream serialisation: the next kernel may start
   // its own set-up now.  Everything below that reads data written by an
@@ -531,10 +552,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     pdl_wait();
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    {
+      SegIter t = make_iter();
+      Segment last, x;
+      while (t.next(x)) { last = x; ++n_segs; }
+      if (SWAP && BN == 16 && n_segs > 0) {
+        int g, ia, ib;
+        tile_coords(last.tile, g, ia, ib);
+        epi_load<SWAP, EPI>(a, g, ia * 128 + row, ib * BN, pre);
+        pre_ok = true;
+      }
+    }
     uint32_t seg = 0;
     SegIter si = make_iter();
     Segment sg;
     while (si.next(sg)) {
+      const bool use_pre = pre_ok && (int)seg == n_segs - 1;
       int g, ia, ib;
       tile_coords(sg.tile, g, ia, ib);
       const uint32_t buf = seg & 1, use = seg >> 1;
@@ -546,6 +579,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
       const int arow = ia * 128 + row;
       const int brow = ib * BN;
+      if (a.cluster_split > 1) {
+        // cluster split-K: park this CTA's piece in its own shared memory (the
+        // operand stages are free: every load was consumed by the finished
+        // MMAs); the cluster's first CTA adds the pieces after the barrier
+        float* red = reinterpret_cast<float*>(smem);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + row] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        ++seg;
+        continue;
+      }
       // pieces of this tile in the stream-K part (1 for a data-parallel tile)
       int nseg = 1, c_first = c;
       int64_t ts = 0;
@@ -559,7 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float v[16];
             EpiIn in;
-            epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+            if (use_pre) in = pre;
+            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
             tmem_ld16(taddr + c0, v);
             tmem_ld_wait();
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
@@ -607,7 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const int64_t tile_k0 = ts * K;
           for (int c0 = 0; c0 < BN; c0 += 16) {
             EpiIn in;
-            epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+            if (use_pre) in = pre;
+            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -638,6 +691,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       ++seg;
     }
+  }
+
+  if (a.cluster_split > 1) {
+    // every thread of the cluster: the pieces are in shared memory
+    cluster_sync();
+    if (cluster_ctarank() == 0 && warp >= 2) {
+      const int row = (warp & 3) * 32 + lane;
+      const int64_t tile = c / a.cluster_split;
+      int g, ia, ib;
+      tile_coords(tile, g, ia, ib);
+      const int arow = ia * 128 + row, brow = ib * BN;
+      const float* red = reinterpret_cast<const float*>(smem);
+      const uint32_t red_s = smem_u32(smem);
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        EpiIn in;
+        if (pre_ok) in = pre;
+        else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = red[(c0 + j) * 128 + row];
+        for (int r = 1; r < a.cluster_split; ++r) {  // pieces in K order
+          float p[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            p[j] = ld_shared_cluster(mapa_shared(red_s + ((c0 + j) * 128 + row) * 4, r));
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += p[j];
+        }
+        epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+      }
+    }
+    cluster_sync();  // keep every piece readable until the sum is done
   }
 
   tc_fence_before();

@@ -62,6 +62,7 @@ struct GemmArgs {
   int a_slice_mid, b_slice_mid;  // 1: tensor map dims are (K, slice, rows)
   int grid;                 // G
   int dp_waves;             // W: tiles [0, W*G) are whole-tile, data-parallel
+  int cluster_split;        // s > 1: cluster of s CTAs per tile, K split s ways (DSMEM sum)
   int64_t total_iters;      // (n_tiles - W*G) * k_slices * k_iters_slice (stream-K part)
   float* partials;          // [G][2][BN][128]
   int* tickets;             // [n_tiles], zero on entry and exit
@@ -95,25 +96,40 @@ struct AttnArgs {
 // on the stream finishes, and waits (griddepcontrol.wait) before touching data
 // a predecessor wrote.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                            cudaStream_t st, Args... args) {
+inline cudaError_t launch_kc(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, int cluster_x, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
+  return launch_kc(kernel, grid, block, smem, st, 1, args...);
 }
 
 // gemm.cu / gemm_epi*.cu
 cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st);
-#define TPK_DECLARE_EPI(E) \
-  cudaError_t launch_gemm_epi##E(bool swap, const GemmArgs& a, size_t smem, cudaStream_t st);
+int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem);
+#define TPK_DECLARE_EPI(E)                                                                   \
+  cudaError_t launch_gemm_epi##E(bool swap, const GemmArgs& a, size_t smem, cudaStream_t st); \
+  int gemm_max_clusters_epi##E(bool swap, int cluster_x, size_t smem);
 TPK_DECLARE_EPI(0)
 TPK_DECLARE_EPI(1)
 TPK_DECLARE_EPI(2)

@@ -173,9 +173,26 @@ GemmPlan plan_gemm(int M) {
 // orientation: whole tiles in data-parallel waves (all CTAs walk K together,
 // so operand slices are shared through L2), and only the tiles of the last
 // partial wave are split stream-K.
-void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms) {
+//
+// Decode orientation with few output tiles: a cluster of s CTAs per tile, each
+// taking 1/s of K, pieces added in K order through distributed shared memory
+// (no global partials, no tail fix-up).  Used when the tiles x s CTAs cover at
+// least 80% of the SMs and all those clusters can be resident at once.
+void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
+  a.cluster_split = 1;
+  if (p.swap) {
+    for (int s = 8; s >= 2; s /= 2) {  // whole TPC pairs: 2, 4 or 8 CTAs
+      if (n_tiles * s > num_sms || n_tiles * s * 5 < (int64_t)num_sms * 4 || K < 2 * s) continue;
+      if (gemm_max_clusters(true, epi, s, p.smem) < n_tiles) continue;
+      a.cluster_split = s;
+      a.dp_waves = 0;
+      a.total_iters = 0;
+      a.grid = (int)(n_tiles * s);
+      return;
+    }
+  }
   if (p.swap || n_tiles < num_sms) {
     a.dp_waves = 0;
     a.total_iters = n_tiles * K;
@@ -295,7 +312,7 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
   a.n_groups = c.t;
   a.k_slices = 1;
   a.k_iters_slice = cdiv(K, 64);
-  set_schedule(a, p, m->num_sms);
+  set_schedule(a, p, m->num_sms, epi);
   a.partials = at<float>(ws, L.gemm_partials);
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
@@ -365,7 +382,7 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
     a.e.out_group_stride = (int64_t)M * H;
     epi = EPI_PARTIAL;
   }
-  set_schedule(a, p, m->num_sms);
+  set_schedule(a, p, m->num_sms, epi);
   TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
   if (!fused) {
     TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {
@@ -417,6 +434,28 @@ struct MapUploader {
 // C ABI
 // ============================================================================
 namespace tpk {
+int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem) {
+  // per (orientation, epilogue, cluster size, smem): the answer never changes
+  static std::mutex mu;
+  static std::vector<std::pair<uint64_t, int>> cache;
+  const uint64_t key = ((uint64_t)smem << 16) | ((uint64_t)cluster_x << 8) | ((uint64_t)epi << 1) |
+                       (swap ? 1u : 0u);
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& kv : cache)
+    if (kv.first == key) return kv.second;
+  int n = 0;
+  switch (epi) {
+    case 0: n = gemm_max_clusters_epi0(swap, cluster_x, smem); break;
+    case 1: n = gemm_max_clusters_epi1(swap, cluster_x, smem); break;
+    case 2: n = gemm_max_clusters_epi2(swap, cluster_x, smem); break;
+    case 3: n = gemm_max_clusters_epi3(swap, cluster_x, smem); break;
+    case 4: n = gemm_max_clusters_epi4(swap, cluster_x, smem); break;
+    case 5: n = gemm_max_clusters_epi5(swap, cluster_x, smem); break;
+  }
+  cache.push_back({key, n});
+  return n;
+}
+
 cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st) {
   switch (epi) {
     case 0: return launch_gemm_epi0(swap, a, smem, st);

@@ -230,3 +230,29 @@ def test_prefill_orientation_schedules_match_oracle(M, inter, t):
     assert rel_err(to_f64(out), ref) <= TOL
     assert m.check_device() == 0
     m.close()
+
+
+@pytest.mark.parametrize("t", [1, 2, 8])
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_decode_cluster_split_matches_oracle(t, M):
+    # hidden 4096: 32 row-parallel output tiles and 48 qkv tiles, which the
+    # decode schedule splits over clusters of CTAs (K pieces summed on chip)
+    w = _wl(hidden=4096, n_heads=32, n_kv=8, head_dim=128, inter=2048)
+    m, _, _ = _model(w, t, head=False)
+    W = oracle_layer(w, 0)
+    x = _x(M, w.hidden, seed=51)
+    dims = O.Dims(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab)
+    p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)
+    y = m.column_linear(0, B.TP_QKV, x)
+    for r, sh in enumerate(O.shard_qkv(W, dims, p)):
+        assert rel_err(to_f64(y[r]), O.linear(to_f64(x), sh)) <= TOL, r
+    for which, Wfull in ((B.TP_O, W.wo), (B.TP_DOWN, W.wd)):
+        a = _x(M, Wfull.shape[1], seed=52)
+        res = _x(M, w.hidden, seed=53)
+        out = m.row_linear_reduce(0, which, a, residual=res, fused=True)
+        ref = O.round_bf16(to_f64(res) + O.linear(to_f64(a), Wfull))
+        assert rel_err(to_f64(out), ref) <= TOL, which
+        again = m.row_linear_reduce(0, which, a, residual=res, fused=True)
+        assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    assert m.check_device() == 0
+    m.close()
