@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--per-t", type=int, default=1)
     p.add_argument("--cpu-baseline", type=int, default=1)
     p.add_argument("--prefill", type=int, default=1)
+    p.add_argument("--configs", type=int, default=1)
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     return p.parse_args()
@@ -58,11 +59,9 @@ def parse():
 # ---------------------------------------------------------------------------
 def layer_bytes(w, t):
     H, d, I = w.hidden, w.head_dim, w.intermediate
-    nkv_r = w.n_kv_heads // t if w.n_kv_heads >= t else 1
-    nq_r = w.n_heads // t
     M = w.tokens
     b = {
-        "gemm_qkv": t * (nq_r + 2 * nkv_r) * d * H * 2 + M * H * 2 + M * (w.n_heads + 2 * w.n_kv_heads) * d * 2,
+        "gemm_qkv": (w.n_heads + 2 * w.n_kv_heads) * d * H * 2 + M * H * 2 + M * (w.n_heads + 2 * w.n_kv_heads) * d * 2,
         "gemm_o": H * w.n_heads * d * 2 + M * w.n_heads * d * 2 + 2 * M * H * 2,
         "gemm_gate_up": 2 * I * H * 2 + M * H * 2 + M * I * 2,
         "gemm_down": H * I * 2 + M * I * 2 + 2 * M * H * 2,
@@ -151,7 +150,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
-def build(w, t, rotate):
+def build(w, t, rotate, head=False):
     import torch
     import synth
     from megatron_tensor_layers_tp_gb300.runtime import TPModel, decode_batch, make_config
@@ -169,8 +168,15 @@ def build(w, t, rotate):
                 synth.fill_normal_(x, w.seed, synth.tensor_id(k, l), w.sigma_w)
             L[k] = x
         layers.append(L)
-    model = TPModel(cfg, layers, max_tokens=w.tokens)
-    del layers
+    emb = fn = lm = None
+    if head:
+        emb = torch.empty((w.vocab, w.hidden), dtype=torch.bfloat16, device="cuda")
+        synth.fill_normal_(emb, w.seed, synth.tensor_id("embed"), w.sigma_w)
+        lm = torch.empty((w.vocab, w.hidden), dtype=torch.bfloat16, device="cuda")
+        synth.fill_normal_(lm, w.seed, synth.tensor_id("lm_head"), w.sigma_w)
+        fn = torch.ones(w.hidden, dtype=torch.bfloat16, device="cuda")
+    model = TPModel(cfg, layers, emb, fn, lm, max_tokens=w.tokens)
+    del layers, emb, lm
     torch.cuda.empty_cache()
     ks, vs = [], []
     for l in range(rotate):
@@ -352,10 +358,16 @@ def run_ours(args, rank, world):
     if args.cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, args.t, args.cpu_budget_s)
     prefill = None
-    if args.prefill and rank == 0 and world == 1:
+    configs = {}
+    if (args.prefill or args.configs) and rank == 0 and world == 1:
         model.close()
         torch.cuda.empty_cache()
+    if args.prefill and rank == 0 and world == 1:
         prefill = prefill_section(stream)
+    if args.configs and rank == 0 and world == 1:
+        for name in ("qwen32b_decode", "qwen32b_decode_kv4"):
+            configs[name] = decode_layer_section(name, stream, hbm_peak)
+        configs["llama8b_full"] = full_forward_section(stream, hbm_peak)
 
     model.close()
     if rank != 0:
@@ -376,7 +388,7 @@ def run_ours(args, rank, world):
                   f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
             "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
             "step_hbm_frac": round(step_gbs / hbm_peak, 3),
-            "per_t": per_t, "kernels": kernels, "prefill": prefill,
+            "per_t": per_t, "kernels": kernels, "prefill": prefill, "decode_configs": configs,
             "kernel_timing": f"CUDA events around each launch on the launch stream, {prof_steps} "
                              f"steps right after the timed region ({ms_prof / prof_steps:.4f} "
                              "ms/step with the events)",
@@ -388,6 +400,95 @@ def run_ours(args, rank, world):
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
+
+
+def kernel_table(prof, kb, hbm_peak):
+    out = {}
+    for name, (n, tot) in prof.items():
+        avg = tot / n
+        e = {"launches": n, "avg_us": round(avg * 1e3, 2)}
+        if name in kb:
+            e["frac_hbm"] = round(kb[name] / (avg * 1e-3) / 1e9 / hbm_peak, 3)
+        out[name] = e
+    return out
+
+
+def decode_layer_section(name, stream, hbm_peak, steps=200, warmup=10):
+    """One Qwen2.5-32B-shaped decoder layer in decode at t = 8: 64 sequences x
+    1 token over a 2048-token KV context (8 KV heads, or 4 shared by replica
+    pairs).  One layer is 1.2-1.5 GB of weights and KV, far above L2."""
+    import torch
+    import synth
+    from megatron_tensor_layers_tp_gb300 import binding as B
+    w = synth.WORKLOADS[name]
+    t = 8
+    with torch.cuda.stream(stream):
+        model, batch, h = build(w, t, 1)
+    ms, _, _ = timed_steps(model, batch, h, steps, warmup, 1, 1, stream)
+    _, prof, _ = timed_steps(model, batch, h, steps // 2, 0, 1, 1, stream, profile=True)
+    assert model.check_device(stream) == 0
+    model.close()
+    del model, batch, h
+    torch.cuda.empty_cache()
+    kb, step_bytes = layer_bytes(w, t)
+    st = ms / steps
+    return {"workload": f"Qwen2.5-32B-shaped decoder layer, decode: {w.n_seqs} sequences x 1 token, "
+                        f"{w.ctx}-token KV context, {w.n_kv_heads} KV heads, t={t}",
+            "tokens_per_s": round(w.tokens / (st * 1e-3), 1), "ms_per_step": round(st, 4),
+            "step_bytes": step_bytes,
+            "step_hbm_frac": round(step_bytes / (st * 1e-3) / 1e9 / hbm_peak, 3),
+            "kernels": kernel_table(prof, kb, hbm_peak)}
+
+
+def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
+    """Llama-3.1-8B-shaped full decode forward at t = 8: vocab-parallel
+    embedding of 64 tokens (one per sequence), 32 layers over a 4096-token KV
+    context, final RMSNorm and the vocab-parallel LM head with the logits
+    gather (49 GB of weights and KV per step)."""
+    import torch
+    import synth
+    from megatron_tensor_layers_tp_gb300 import binding as B
+    w = synth.WORKLOADS["llama8b_full"]
+    t = 8
+    with torch.cuda.stream(stream):
+        model, batch, _ = build(w, t, w.n_layers, head=True)
+        ids = torch.empty(w.tokens, dtype=torch.int32, device="cuda")
+        synth.fill_uniform_(ids, w.seed, synth.tensor_id("ids"), w.vocab)
+        hbuf = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
+        logits = torch.empty((w.n_seqs, w.vocab), dtype=torch.bfloat16, device="cuda")
+        cb = batch.to_c()
+    torch.cuda.synchronize()
+
+    def run(n):
+        for _ in range(n):
+            model.forward(ids, batch, stream=stream, h=hbuf, logits=logits, cbatch=cb)
+    run(warmup)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(reps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    B.tp_profile(model.handle, True)
+    run(2)
+    B.tp_profile(model.handle, False)
+    prof = B.tp_profile_read(model.handle, stream.cuda_stream)
+    assert model.check_device(stream) == 0
+    model.close()
+    del model, batch
+    torch.cuda.empty_cache()
+    kb, lb = layer_bytes(w, t)
+    kb = dict(kb)
+    kb["gemm_lm_head"] = w.vocab * w.hidden * 2 + w.tokens * w.hidden * 2 + w.tokens * w.vocab * 2
+    kb["embed"] = 2 * w.tokens * w.hidden * 2
+    step_bytes = w.n_layers * lb + kb["gemm_lm_head"] + kb["embed"] + w.tokens * w.hidden * 4
+    return {"workload": "Llama-3.1-8B-shaped full decode forward: 64 sequences x 1 token, 4096-token "
+                        "KV context, 32 layers + embedding + LM head, t=8",
+            "tokens_per_s": round(w.tokens / (ms * 1e-3), 1), "ms_per_forward": round(ms, 4),
+            "step_bytes": step_bytes,
+            "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
+            "kernels": kernel_table(prof, kb, hbm_peak)}
 
 
 def prefill_section(stream, reps=10):

@@ -199,7 +199,10 @@ enum { TP_DECODE = 0, TP_PREFILL = 1 };
  * g (local to the copy), position p, element e lives at
  *   base[(((c*n_seqs + b)*kv_heads_per_rank + g)*l_max + p)*head_dim + e]
  * Replica ranks (n_kv < t) share copy c = r / kv_replicas.  The layer writes
- * each token's K and V at its position before attention reads them. */
+ * each token's K and V at its position before attention reads them; the rows
+ * below a token's position must already hold their values when the call is
+ * enqueued (written earlier in stream order), since decode attention may start
+ * reading them while the kernels before it are still running. */
 typedef struct {
   int32_t mode;                /* TP_DECODE or TP_PREFILL */
   int32_t n_seqs;

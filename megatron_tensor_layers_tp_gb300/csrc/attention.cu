@@ -164,16 +164,26 @@ __device__ __forceinline__ void load_q_frags(uint32_t sQ, int row_bytes, uint32_
 // ============================================================================
 // decode
 // ============================================================================
-constexpr int kDecWarps = 4;                       // compute warps
-constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + producer warp
+// Two groups of four compute warps take alternate 64-key tiles (each warp 16
+// keys of its group's tile), so two tiles are in the mma/softmax chain at once.
+constexpr int kDecGroupWarps = 4;
+constexpr int kDecGroups = 2;
+constexpr int kDecWarps = kDecGroups * kDecGroupWarps;  // compute warps
+constexpr int kDecThreads = (kDecWarps + 1) * 32;        // + producer warp
 
 template <int D>
 struct DecSmem {
   static constexpr int kTileBytes = (D / 64) * 8192;       // one K or V tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kQRow = D * 2 + 16;                 // padded bf16 row
-  static constexpr int kStages = D == 128 ? 5 : 8;
-  static constexpr int kComb = kDecWarps * 16 * (D + 2);   // floats: O, m, l per warp/row
+  // An even stage count pins every stage to one warp group inside a segment
+  // (stage n % S, group n % 2 relative to the segment's first unit), so a
+  // group never waits on a stage whose previous fill, owned by the other
+  // group, is still in flight (an mbarrier parity wait cannot tell that fill
+  // from the one it wants).
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static_assert(kStages % kDecGroups == 0, "stages must split evenly between the warp groups");
+  static constexpr int kComb = kDecGroupWarps * 16 * (D + 2);  // floats: O, m, l per warp/row
   static constexpr size_t bytes(int) {
     return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
   }
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = L::kStages;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDecWarps); }
+    for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDecGroupWarps); }
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -207,7 +217,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   }
   __syncthreads();
   pdl_launch_dependents();
-  pdl_wait();  // q and the cache rows were written by the preceding kernels
 
   const int G = a.grid, c = blockIdx.x;
   const int64_t T = a.total_units;
@@ -222,14 +231,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       const int64_t bg0 = beg / TB;
       int tile = static_cast<int>(beg - bg0 * TB);
       int b = static_cast<int>(bg0 / a.n_kv), g = static_cast<int>(bg0 % a.n_kv);
-      for (int64_t u = beg; u < end; ++u) {
-        if (u != beg && ++tile == TB) {
-          tile = 0;
-          if (++g == a.n_kv) { g = 0; ++b; }
-        }
+      auto issue = [&](uint32_t s) {
         const int slice = ((g / a.kv_r) * a.n_seqs + b) * a.kv_r + (g % a.kv_r);
-        const uint32_t s = n % S, ph = (n / S) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
         mbar_arrive_expect_tx(&full[s], L::kStageBytes);
         uint8_t* kt = tiles + s * L::kStageBytes;
 #pragma unroll
@@ -238,13 +241,40 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
           tma_load_3d(kt + L::kTileBytes + bx * 8192, &a.tmV, &full[s], bx * 64, tile * kKeyTile,
                       slice, pol);
         }
+      };
+      auto advance = [&]() {
+        if (++tile == TB) {
+          tile = 0;
+          if (++g == a.n_kv) { g = 0; ++b; }
+        }
+      };
+      // Cache rows below a sequence's position were written before this
+      // launch chain: the qkv projection that writes this step's rows signals
+      // its dependents only after its own wait, so every kernel older than it
+      // has completed.  Tiles wholly below the position therefore fill the
+      // first stages before the wait for q and the new rows.
+      int64_t u = beg;
+      while (u < end && n < (uint32_t)S && (tile + 1) * kKeyTile <= a.positions[b]) {
+        issue(n);
         ++n;
+        if (++u < end) advance();
+      }
+      pdl_wait();
+      for (; u < end; ++u) {
+        const uint32_t s = n % S, ph = (n / S) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, a.status)) break;
+        issue(s);
+        ++n;
+        if (u + 1 < end) advance();
       }
       for (uint32_t i = (n > (uint32_t)S ? n - S : 0); i < n; ++i)
         mbar_wait(&full[i % S], (i / S) & 1, a.status);
+    } else {
+      pdl_wait();
     }
   } else {
-    const int ctid = threadIdx.x;  // 0..127
+    pdl_wait();  // q and the newest cache rows were written by the preceding kernels
+    const int ctid = threadIdx.x;  // 0..255
     uint32_t n_base = 0;           // CTA-local index of the segment's first unit
     bool alive = true;
     for (int64_t u0 = beg; u0 < end;) {
@@ -273,59 +303,104 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
       const int lim[2] = {pos, pos};
-      // every warp takes its own 16 keys of every 64-key tile, so a stage is
-      // released after a quarter of the work and the other stages keep
-      // streaming
-      for (int i = 0; i < len; ++i) {
+      // group grp takes tiles grp, grp + 2, ... of the segment; every warp of
+      // it takes its own 16 keys of the tile, so a stage is released after a
+      // quarter of that tile's work and the other stages keep streaming
+      const int grp = warp / kDecGroupWarps, wq = warp % kDecGroupWarps;
+      constexpr int kWarpKeys = kKeyTile / kDecGroupWarps;
+      for (int i = grp; i < len; i += kDecGroups) {
         const uint32_t n = n_base + i;
         const uint32_t s = n % S, ph = (n / S) & 1;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&full[s], ph, a.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { alive = false; break; }
-        const int key0 = (tile0 + i) * kKeyTile + warp * (kKeyTile / kDecWarps);
+        const int key0 = (tile0 + i) * kKeyTile + wq * kWarpKeys;
         if (key0 <= pos) {
           const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
-          attn_tile<D, kKeyTile / kDecWarps / 8>(qa, st, st + L::kTileBytes,
-                                                 warp * (kKeyTile / kDecWarps), key0, lim,
-                                                 a.scale_log2, m, l, o);
+          attn_tile<D, kWarpKeys / 8>(qa, st, st + L::kTileBytes, wq * kWarpKeys, key0, lim,
+                                      a.scale_log2, m, l, o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       n_base += len;
-      // combine the 4 warps' (m, l, O) in smem
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
       }
-      float* cw = comb + warp * 16 * (D + 2);
+      // combine: the second group's (m, l, O) is folded into the first
+      // group's registers (same fragment layout), then the four merged
+      // states meet in smem
+      float* cw = comb + wq * 16 * (D + 2);
       const int r0 = lane >> 2;
+      if (grp == 1) {
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        const int col = nt * 8 + (lane & 3) * 2;
-        cw[r0 * (D + 2) + col] = o[nt][0];
-        cw[r0 * (D + 2) + col + 1] = o[nt][1];
-        cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
-        cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
+        for (int nt = 0; nt < D / 8; ++nt) {
+          const int col = nt * 8 + (lane & 3) * 2;
+          cw[r0 * (D + 2) + col] = o[nt][0];
+          cw[r0 * (D + 2) + col + 1] = o[nt][1];
+          cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
+          cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
+        }
+        if ((lane & 3) == 0) {
+          cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
+          cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
+        }
       }
-      if ((lane & 3) == 0) {
-        cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
-        cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
+      bar_sync(1, kDecWarps * 32);
+      if (grp == 0) {
+        float sa[2], sb[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float mb = cw[(r0 + 8 * h) * (D + 2) + D];
+          const float lb = cw[(r0 + 8 * h) * (D + 2) + D + 1];
+          const float mn = fmaxf(m[h], mb);
+          sa[h] = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mn);
+          sb[h] = mb == -INFINITY ? 0.f : exp2f(mb - mn);
+          l[h] = l[h] * sa[h] + lb * sb[h];
+          m[h] = mn;
+        }
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          const int col = nt * 8 + (lane & 3) * 2;
+          o[nt][0] = o[nt][0] * sa[0] + cw[r0 * (D + 2) + col] * sb[0];
+          o[nt][1] = o[nt][1] * sa[0] + cw[r0 * (D + 2) + col + 1] * sb[0];
+          o[nt][2] = o[nt][2] * sa[1] + cw[(r0 + 8) * (D + 2) + col] * sb[1];
+          o[nt][3] = o[nt][3] * sa[1] + cw[(r0 + 8) * (D + 2) + col + 1] * sb[1];
+        }
+      }
+      bar_sync(1, kDecWarps * 32);
+      if (grp == 0) {
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          const int col = nt * 8 + (lane & 3) * 2;
+          cw[r0 * (D + 2) + col] = o[nt][0];
+          cw[r0 * (D + 2) + col + 1] = o[nt][1];
+          cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
+          cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
+        }
+        if ((lane & 3) == 0) {
+          cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
+          cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
+        }
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
-      // 128 threads: row = ctid / 8, 16 columns each (D = 128) or 8 (D = 64)
+      // row = ct / 8, 16 columns each (D = 128) or 8 (D = 64); the second
+      // group's threads repeat the first group's arithmetic and store nothing
       constexpr int CPT = D / 8;
-      const int row = ctid >> 3, c0 = (ctid & 7) * CPT;
+      const bool cthr = ctid < kDecGroupWarps * 32;
+      const int ct = ctid & (kDecGroupWarps * 32 - 1);
+      const int row = ct >> 3, c0 = (ct & 7) * CPT;
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
+      for (int w = 0; w < kDecGroupWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
       float ll = 0.f, acc[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
+      for (int w = 0; w < kDecGroupWarps; ++w) {
         const float* cr = comb + (w * 16 + row) * (D + 2);
         const float mw = cr[D];
         if (mw == -INFINITY) continue;
@@ -337,7 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
       uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + c0;
       if (nseg == 1) {
-        if (row < a.group) {
+        if (cthr && row < a.group) {
           const float inv = 1.f / ll;
 #pragma unroll
           for (int j = 0; j < CPT; j += 8) {
@@ -352,9 +427,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         const int first_c = owner_of(bg * TB, T, G);
         const int my_slot = (beg / TB == bg) ? 0 : 1;
         float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
+        if (cthr) {
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
-        if ((ctid & 7) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
+          for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
+          if ((ct & 7) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
+        }
         __threadfence();
         bar_sync(1, kDecWarps * 32);
         if (ctid == 0) {
@@ -385,7 +462,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + c0 + j]) * sc;
           }
-          if (row < a.group) {
+          if (cthr && row < a.group) {
             const float inv = 1.f / L2;
 #pragma unroll
             for (int j = 0; j < CPT; j += 8) {

@@ -66,9 +66,11 @@ __device__ __forceinline__ int plain_col(const EpiArgs& e, int f) {
   return base + ((w & 1) ? (w >> 1) + d / 2 : (w >> 1));
 }
 
-// Global inputs of the decode-orientation epilogues (residual values; token
-// positions, sequences and RoPE factors), fetched by epi_load ahead of the
-// arithmetic so their latency overlaps the other loads of a fix-up.
+// Inputs of the epilogues (residual values; token positions, sequences and
+// RoPE factors), fetched by epi_load ahead of the arithmetic so their latency
+// overlaps the other loads of a fix-up.  In the decode orientation positions
+// and sequences come from the CTA's shared-memory copy (tok: positions of
+// tokens 0..kSwapMaxTokens-1, then their sequences).
 struct EpiIn {
   float r[16];
   int pos[16];
@@ -77,7 +79,8 @@ struct EpiIn {
 };
 
 template <bool SWAP, int EPI>
-__device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int brow0, EpiIn& in) {
+__device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int brow0,
+                                         const int* tok, EpiIn& in) {
   const EpiArgs& e = a.e;
   const int f = arow;
   const bool fval = f < a.a_rows_valid;
@@ -96,8 +99,8 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
     for (int j = 0; j < 16; ++j) {
       const int m = brow0 + j;
       const bool ok = fval && m < e.M;
-      in.pos[j] = ok ? e.positions[m] : -1;
-      in.seq[j] = (ok && kind != 0) ? e.token_seq[m] : 0;
+      in.pos[j] = ok ? tok[m] : -1;
+      in.seq[j] = (ok && kind != 0) ? tok[kSwapMaxTokens + m] : 0;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -404,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* tok = reinterpret_cast<int*>(last_flag + 3);  // decode: token positions, then sequences
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -451,8 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   // Launched with programmatic stream serialisation: the next kernel may start
   // its own set-up now.  Everything below that reads data written by an
   // earlier kernel comes after pdl_wait(); only the weight shards (written
-  // once when the model was loaded) are fetched before it.
-  pdl_launch_dependents();
+  // once when the model was loaded) are fetched before it.  The qkv
+  // projection is the exception that signals late (after its wait): decode
+  // attention reads the cache rows of earlier steps before its own wait, which
+  // is sound only if every kernel before this one has completed.
+  if constexpr (EPI != EPI_QKV) pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
@@ -550,16 +557,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     pdl_wait();
+    if constexpr (EPI == EPI_QKV) pdl_launch_dependents();
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
+    if constexpr (SWAP && EPI == EPI_QKV) {
+      // every tile of the decode orientation covers tokens 0..M-1
+      if (et < kSwapMaxTokens) {
+        const bool ok = et < a.e.M;
+        tok[et] = ok ? a.e.positions[et] : -1;
+        tok[kSwapMaxTokens + et] = ok ? a.e.token_seq[et] : 0;
+      }
+      bar_sync(1, 128);
+    }
+    // chunks of 16 columns this CTA finishes itself: all of them, except in a
+    // cluster split where rank r sums and stores chunks r, r + s, ...
+    const int rank = a.cluster_split > 1 ? static_cast<int>(c % a.cluster_split) : 0;
+    const int chunk0 = a.cluster_split > 1 ? rank * 16 : 0;
+    const int chunk_step = a.cluster_split > 1 ? a.cluster_split * 16 : 16;
     {
       SegIter t = make_iter();
       Segment last, x;
       while (t.next(x)) { last = x; ++n_segs; }
-      if (SWAP && BN == 16 && n_segs > 0) {
+      if (SWAP && n_segs > 0 && chunk0 < BN) {
         int g, ia, ib;
         tile_coords(last.tile, g, ia, ib);
-        epi_load<SWAP, EPI>(a, g, ia * 128 + row, ib * BN, pre);
+        epi_load<SWAP, EPI>(a, g, ia * 128 + row, ib * BN + chunk0, tok, pre);
         pre_ok = true;
       }
     }
@@ -582,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (a.cluster_split > 1) {
         // cluster split-K: park this CTA's piece in its own shared memory (the
         // operand stages are free: every load was consumed by the finished
-        // MMAs); the cluster's first CTA adds the pieces after the barrier
+        // MMAs); the pieces are summed after the cluster barrier
         float* red = reinterpret_cast<float*>(smem);
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
@@ -610,8 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float v[16];
             EpiIn in;
-            if (use_pre) in = pre;
-            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+            if (use_pre && c0 == 0) in = pre;
+            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
             tmem_ld16(taddr + c0, v);
             tmem_ld_wait();
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
@@ -619,9 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         } else {
           // inputs of chunk c0 + 16 are fetched before chunk c0 is stored
           EpiIn cur, nxt;
-          epi_load<SWAP, EPI>(a, g, arow, brow, cur);
+          epi_load<SWAP, EPI>(a, g, arow, brow, tok, cur);
           for (int c0 = 0; c0 < BN; c0 += 16) {
-            if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, nxt);
+            if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
             float v[16];
             tmem_ld16(taddr + c0, v);
             tmem_ld_wait();
@@ -655,33 +678,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         bar_sync(1, 128);
         if (*last_flag) {
           __threadfence();
-          // the pieces in K order; loads of 4 pieces are issued before their adds
-          const int64_t tile_k0 = ts * K;
+          // The pieces in K order are those of CTAs c_first, c_first + 1, ...;
+          // only the first can have started its range before this tile (its
+          // piece then sits in slot 1).  Loads of up to 4 pieces are in flight
+          // together, and the first batch of the next chunk is fetched before
+          // the current chunk is stored.
+          const int slot0 = range_begin(c_first, T, G) == ts * K ? 0 : 1;
+          const float* base = a.partials + (int64_t)c_first * 2 * BN * 128 + row;
+          float tmp[4][16];
+          auto load_batch = [&](int c0, int s0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (s0 + q < nseg) {
+                const int pq = s0 + q;
+                const float* src = base + ((int64_t)pq * 2 + (pq == 0 ? slot0 : 0)) * BN * 128 +
+                                   c0 * 128;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) tmp[q][j] = __ldcg(src + j * 128);
+              }
+            }
+          };
+          load_batch(0, 0);
           for (int c0 = 0; c0 < BN; c0 += 16) {
             EpiIn in;
-            if (use_pre) in = pre;
-            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+            if (use_pre && c0 == 0) in = pre;
+            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
             for (int s0 = 0; s0 < nseg; s0 += 4) {
-              float tmp[4][16];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int cc = c_first + s0 + q;
-                if (s0 + q < nseg) {
-                  const int slot = range_begin(cc, T, G) >= tile_k0 ? 0 : 1;
-                  const float* src = a.partials + ((int64_t)(cc * 2 + slot) * BN) * 128;
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) tmp[q][j] = __ldcg(&src[(c0 + j) * 128 + row]);
-                }
-              }
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 if (s0 + q < nseg) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j) v[j] += tmp[q][j];
                 }
+              if (s0 + 4 < nseg) load_batch(c0, s0 + 4);
+              else if (c0 + 16 < BN) load_batch(c0 + 16, 0);
             }
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
           }
@@ -696,33 +729,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (a.cluster_split > 1) {
     // every thread of the cluster: the pieces are in shared memory
     cluster_sync();
-    if (cluster_ctarank() == 0 && warp >= 2) {
+    if (warp >= 2) {
+      const int rank = static_cast<int>(c % a.cluster_split);
       const int row = (warp & 3) * 32 + lane;
       const int64_t tile = c / a.cluster_split;
       int g, ia, ib;
       tile_coords(tile, g, ia, ib);
       const int arow = ia * 128 + row, brow = ib * BN;
-      const float* red = reinterpret_cast<const float*>(smem);
       const uint32_t red_s = smem_u32(smem);
-      for (int c0 = 0; c0 < BN; c0 += 16) {
+      // rank r sums and stores chunks r, r + s, ...; the pieces are added in
+      // K order (rank 0 first), up to 4 remote loads in flight together
+      for (int c0 = rank * 16; c0 < BN; c0 += a.cluster_split * 16) {
         EpiIn in;
-        if (pre_ok) in = pre;
-        else epi_load<SWAP, EPI>(a, g, arow, brow + c0, in);
+        if (pre_ok && c0 == rank * 16) in = pre;
+        else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
         float v[16];
+        for (int r0 = 0; r0 < a.cluster_split; r0 += 4) {
+          float p[4][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = red[(c0 + j) * 128 + row];
-        for (int r = 1; r < a.cluster_split; ++r) {  // pieces in K order
-          float p[16];
+          for (int q = 0; q < 4; ++q)
+            if (r0 + q < a.cluster_split) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            p[j] = ld_shared_cluster(mapa_shared(red_s + ((c0 + j) * 128 + row) * 4, r));
+              for (int j = 0; j < 16; ++j)
+                p[q][j] = ld_shared_cluster(mapa_shared(red_s + ((c0 + j) * 128 + row) * 4, r0 + q));
+            }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += p[j];
+          for (int q = 0; q < 4; ++q)
+            if (r0 + q < a.cluster_split) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = (r0 + q == 0) ? p[q][j] : v[j] + p[q][j];
+            }
         }
         epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
       }
     }
-    cluster_sync();  // keep every piece readable until the sum is done
+    cluster_sync();  // keep every piece readable until the sums are done
   }
 
   tc_fence_before();

@@ -8,6 +8,10 @@
 
 namespace tpk {
 
+// Decode orientation (tokens on the MMA N side) for at most this many tokens;
+// the GEMM keeps their positions and sequences in shared memory.
+constexpr int kSwapMaxTokens = 64;
+
 enum Epi : int {
   EPI_PLAIN = 0,    // column-parallel output, standard per-rank order
   EPI_QKV = 1,      // RoPE on q,k; q -> q buffer, k,v -> rank cache

@@ -52,7 +52,6 @@ struct tp_model {
 namespace {
 
 constexpr int kPrefillBN = 256;
-constexpr int kSwapMaxTokens = 64;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -164,7 +163,7 @@ GemmPlan plan_gemm(int M) {
   int cols = 32;
   while (cols < 2 * p.BN) cols *= 2;
   p.tmem_cols = cols;
-  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16;
+  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 2 * kSwapMaxTokens * 4;
   return p;
 }
 
@@ -183,7 +182,10 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
   a.cluster_split = 1;
   if (p.swap) {
-    for (int s = 8; s >= 2; s /= 2) {  // whole TPC pairs: 2, 4 or 8 CTAs
+    // the largest cluster (8 CTAs at most, portable) whose tiles x s CTAs fill
+    // at least 80% of the SMs in one wave; the occupancy query decides
+    // whether that many clusters are co-resident on this part's GPCs
+    for (int s = 8; s >= 2; --s) {
       if (n_tiles * s > num_sms || n_tiles * s * 5 < (int64_t)num_sms * 4 || K < 2 * s) continue;
       if (gemm_max_clusters(true, epi, s, p.smem) < n_tiles) continue;
       a.cluster_split = s;
