@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--cpu-baseline", type=int, default=1)
     p.add_argument("--prefill", type=int, default=1)
     p.add_argument("--configs", type=int, default=1)
+    p.add_argument("--prefill-only", type=int, default=0,
+                   help="profiling aid: run only the prefill section and print its JSON")
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     return p.parse_args()
@@ -70,6 +72,27 @@ def layer_bytes(w, t):
     }
     total = sum(b.values()) + b["rmsnorm"]  # two norms per layer
     return b, total
+
+
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the CUDA sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    d = os.path.join(ROOT, "megatron_tensor_layers_tp_gb300", "csrc")
+    h = hashlib.sha256()
+    for n in sorted(os.listdir(d)):
+        h.update(n.encode())
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("csrc_sha256"):
+        return None
+    k = rec.get("kernels", {}).get(kernel)
+    return k["dram_bytes_per_launch"] if k else None
 
 
 def read_peaks():
@@ -290,7 +313,8 @@ def run_ours(args, rank, world):
         avg_s = tot / n * 1e-3
         ach = kb[dom] / avg_s / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
-                    "unit": "GB/s", "frac": round(ach / hbm_peak, 3), "traffic": None,
+                    "unit": "GB/s", "frac": round(ach / hbm_peak, 3),
+                    "traffic": measured_traffic(dom),
                     "algorithmic_bytes": kb[dom], "peak_source": peak_src}
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
 
@@ -669,6 +693,11 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.prefill_only:
+        import torch
+        stream = torch.cuda.Stream()
+        print(json.dumps({"prefill": prefill_section(stream)}), flush=True)
         return
     if world > 1:
         import torch
