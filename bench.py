@@ -318,6 +318,23 @@ def run_ours(args, rank, world):
                     "algorithmic_bytes": kb[dom], "peak_source": peak_src}
     step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
 
+    # the same steps replayed from CUDA graphs (one per rotating layer)
+    graphs = [model.capture_layer(l, batch, h, stream, fused=bool(args.fused))
+              for l in range(args.rotate)]
+    n_g = max(min(args.steps, 2000), 20)
+    for i in range(args.warmup):
+        graphs[i % args.rotate].launch(stream)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(n_g):
+        graphs[i % args.rotate].launch(stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph_step = g0.elapsed_time(g1) / n_g
+    for g in graphs:
+        g.close()
+
     # t = 1, 2, 4 beside the headline
     per_t = {}
     if args.per_t and rank == 0 and world == 1:
@@ -411,6 +428,7 @@ def run_ours(args, rank, world):
             "l2": f"inputs larger than L2: steps rotate over {args.rotate} layers with distinct "
                   f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
             "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
+            "ms_per_step_cuda_graph": round(ms_graph_step, 5),
             "step_hbm_frac": round(step_gbs / hbm_peak, 3),
             "per_t": per_t, "kernels": kernels, "prefill": prefill, "decode_configs": configs,
             "kernel_timing": f"CUDA events around each launch on the launch stream, {prof_steps} "
@@ -498,6 +516,17 @@ def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
     run(2)
     B.tp_profile(model.handle, False)
     prof = B.tp_profile_read(model.handle, stream.cuda_stream)
+    # the same forward replayed from one CUDA graph
+    graph = model.capture_forward(ids, batch, hbuf, logits, stream, cbatch=cb)
+    for _ in range(warmup):
+        graph.launch(stream)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph = e0.elapsed_time(e1) / reps
+    graph.close()
     assert model.check_device(stream) == 0
     model.close()
     del model, batch
@@ -510,6 +539,7 @@ def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
     return {"workload": "Llama-3.1-8B-shaped full decode forward: 64 sequences x 1 token, 4096-token "
                         "KV context, 32 layers + embedding + LM head, t=8",
             "tokens_per_s": round(w.tokens / (ms * 1e-3), 1), "ms_per_forward": round(ms, 4),
+            "ms_per_forward_cuda_graph": round(ms_graph, 4),
             "step_bytes": step_bytes,
             "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
             "kernels": kernel_table(prof, kb, hbm_peak)}

@@ -241,6 +241,68 @@ tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
                      tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
                      size_t ws_bytes, void* stream);
 
+/* One pipeline stage (P3 流水线并行: the layers are cut into consecutive groups,
+ * each stage builds only its own layers, and a non-final stage hands its
+ * running hidden state to the next).  Runs layers
+ * [first_layer, first_layer + n_layers) on h in place.
+ *   ids    : non-NULL on the first stage only: h = vocab-parallel embedding of
+ *            ids [n_tokens] before the layers (first_layer must then be 0).
+ *   logits : non-NULL on the last stage only: final RMSNorm of the sampled rows
+ *            and the vocab-parallel LM head with the logits gather, as
+ *            tp_forward (first_layer + n_layers must then be n_layers of the
+ *            model; ld_logits >= vocab).
+ * Stages covering layers 0..n_layers-1 in order, joined by tp_stage_send,
+ * launch the same kernels in the same order as tp_forward and return its
+ * logits bit for bit.  Errors: TP_ERR_ARG for a layer range outside the model
+ * or the conditions above; otherwise as tp_forward. */
+tp_status tp_stage_forward(const tp_model* m, int32_t first_layer, int32_t n_layers,
+                           const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
+                           tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Stage-boundary hand-off (P3 流水线并行).  Copies the running hidden state
+ * [M, H] bf16 from one stage's buffer (src) to the next stage's (dst).  With
+ * tensor parallelism inside each stage, rank r sends only its slice of
+ * columns [r H/t, (r+1) H/t) and the receiving stage all-gathers the slices
+ * inside its TP group; here one kernel moves the t slices and they land side
+ * by side in dst, which is that all-gather's result.
+ * Counters: stage_sends += 1, stage_send_bytes += M*H*2 (M*H*2/t per rank).
+ * The pages estimate 2 x H x 2 bytes per token because their engines hand
+ * over the hidden state and the residual as two tensors; this library adds
+ * the residual inside the row-parallel epilogues, so one tensor of H x 2
+ * bytes per token carries both.
+ * Requires (H / t) % 8 == 0, 16-byte aligned src and dst that do not overlap;
+ * TP_ERR_ARG otherwise. */
+tp_status tp_stage_send(const tp_model* m, const tp_bf16* src, tp_bf16* dst, int32_t M,
+                        void* stream);
+
+/* CUDA-graph capture of one decode step (P3 每 token 的通信量 读法: a fixed cost
+ * per synchronisation that "custom all-reduce and CUDA graph" address; P1
+ * names CUDA graph among the engines' decode optimisations).
+ * tp_graph_capture_forward / tp_graph_capture_layer record the kernels that
+ * tp_forward / tp_layer_forward would launch with these arguments, on
+ * `stream` (a stream the caller created, not the legacy default stream), into
+ * an executable graph; nothing runs during the capture.  tp_graph_launch
+ * replays it on any stream.  A replay reads the current contents of every
+ * buffer the captured call named (ids, positions, caches, h, workspace), so
+ * the caller refreshes their contents between replays but keeps their
+ * addresses, the batch shape and the workspace alive and unshared while the
+ * graph exists.  Each replay adds the captured call's counters to the model's
+ * (tp_get_stats).  Errors: TP_ERR_ARG for a NULL stream or output pointer or
+ * while tp_profile is enabled; the captured call's own argument errors;
+ * TP_ERR_CUDA if capture or instantiation fails (the stream is left out of
+ * capture mode). */
+typedef struct tp_graph tp_graph;
+tp_status tp_graph_capture_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
+                                   tp_bf16* h, tp_bf16* logits, int64_t ld_logits,
+                                   int32_t fused, void* ws, size_t ws_bytes, void* stream,
+                                   tp_graph** out);
+tp_status tp_graph_capture_layer(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                                 tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
+                                 void* stream, tp_graph** out);
+tp_status tp_graph_launch(tp_graph* g, void* stream);
+void tp_graph_free(tp_graph* g);
+
 /* tp_row_linear_reduce with fused = 1, for callers that cannot allocate
  * device memory — for example a plug-in that its host framework hands only
  * input and output tensors, or a latency-critical loop that cannot afford
@@ -284,6 +346,8 @@ typedef struct {
   int64_t allgathers;          /* logits gathers */
   int64_t allgather_recv_bytes_per_rank;
   int64_t kernel_launches;     /* kernels launched by the library */
+  int64_t stage_sends;         /* pipeline-stage boundaries crossed (tp_stage_send) */
+  int64_t stage_send_bytes;    /* bytes handed across them, all ranks together */
 } tp_stats_t;
 
 tp_status tp_get_stats(const tp_model* m, tp_stats_t* out);

@@ -52,7 +52,8 @@ class tp_batch_t(Structure):
 
 class tp_stats_t(Structure):
     _fields_ = [(n, c_int64) for n in ("allreduces", "allreduce_payload_bytes", "allgathers",
-                                       "allgather_recv_bytes_per_rank", "kernel_launches")]
+                                       "allgather_recv_bytes_per_rank", "kernel_launches",
+                                       "stage_sends", "stage_send_bytes")]
 
 
 class tp_kernel_time_t(Structure):
@@ -88,6 +89,17 @@ _SIGS = {
                                    c_void_p, c_size_t, c_void_p]),
     "tp_forward": (c_int32, [c_void_p, c_void_p, POINTER(tp_batch_t), c_void_p, c_void_p, c_int64,
                              c_int32, c_void_p, c_size_t, c_void_p]),
+    "tp_stage_forward": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, POINTER(tp_batch_t),
+                                   c_void_p, c_void_p, c_int64, c_int32, c_void_p, c_size_t,
+                                   c_void_p]),
+    "tp_stage_send": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p]),
+    "tp_graph_capture_forward": (c_int32, [c_void_p, c_void_p, POINTER(tp_batch_t), c_void_p,
+                                           c_void_p, c_int64, c_int32, c_void_p, c_size_t,
+                                           c_void_p, POINTER(c_void_p)]),
+    "tp_graph_capture_layer": (c_int32, [c_void_p, c_int32, POINTER(tp_batch_t), c_void_p, c_int32,
+                                         c_void_p, c_size_t, c_void_p, POINTER(c_void_p)]),
+    "tp_graph_launch": (c_int32, [c_void_p, c_void_p]),
+    "tp_graph_free": (None, [c_void_p]),
     "tp_row_linear_reduce_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int64,
                                                c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
     "tp_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
@@ -198,6 +210,41 @@ def tp_forward(model, ids, batch: tp_batch_t, h, logits, ld_logits, fused, ws, w
                stream) -> int:
     return lib().tp_forward(model, ids, ctypes.byref(batch), h, logits, ld_logits, fused, ws,
                             ws_bytes, stream)
+
+
+def tp_stage_forward(model, first_layer, n_layers, ids, batch: tp_batch_t, h, logits, ld_logits,
+                     fused, ws, ws_bytes, stream) -> int:
+    return lib().tp_stage_forward(model, first_layer, n_layers, ids, ctypes.byref(batch), h, logits,
+                                  ld_logits, fused, ws, ws_bytes, stream)
+
+
+def tp_stage_send(model, src, dst, M, stream) -> int:
+    return lib().tp_stage_send(model, src, dst, M, stream)
+
+
+def tp_graph_capture_forward(model, ids, batch: tp_batch_t, h, logits, ld_logits, fused, ws,
+                             ws_bytes, stream):
+    """Returns (status, graph handle)."""
+    g = c_void_p()
+    st = lib().tp_graph_capture_forward(model, ids, ctypes.byref(batch), h, logits, ld_logits,
+                                        fused, ws, ws_bytes, stream, ctypes.byref(g))
+    return st, g.value
+
+
+def tp_graph_capture_layer(model, layer, batch: tp_batch_t, h, fused, ws, ws_bytes, stream):
+    """Returns (status, graph handle)."""
+    g = c_void_p()
+    st = lib().tp_graph_capture_layer(model, layer, ctypes.byref(batch), h, fused, ws, ws_bytes,
+                                      stream, ctypes.byref(g))
+    return st, g.value
+
+
+def tp_graph_launch(graph, stream) -> int:
+    return lib().tp_graph_launch(graph, stream)
+
+
+def tp_graph_free(graph) -> None:
+    lib().tp_graph_free(graph)
 
 
 def tp_rmsnorm(model, x, w, M, y, stream) -> int:

@@ -159,5 +159,7 @@ cudaError_t launch_rope_table(float2* table, int max_pos, int head_dim, double t
                               cudaStream_t st);
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st);
+cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, int t,
+                              cudaStream_t st);
 
 }  // namespace tpk

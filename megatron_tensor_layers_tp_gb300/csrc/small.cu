@@ -202,6 +202,29 @@ __global__ void copy_rows_kernel(uint16_t* __restrict__ dst, int64_t dst_ld,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pipeline-stage hand-off ("张量、流水线与数据并行", 流水线并行): CTA (row i,
+// rank r) moves rank r's slice of columns [r H/t, (r+1) H/t) of hidden row i
+// into the next stage's buffer, where the t slices land side by side (the
+// receiving stage's all-gather inside its TP group).  16-byte vectors;
+// (H/t) % 8 == 0 is checked by the host.
+// ---------------------------------------------------------------------------
+__global__ void stage_send_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                  int H, int slice) {
+  pdl_launch_dependents();
+  pdl_wait();  // the sending stage's last kernel wrote src
+  const int64_t off = (int64_t)blockIdx.x * H + (int64_t)blockIdx.y * slice;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + off);
+  uint4* d4 = reinterpret_cast<uint4*>(dst + off);
+  for (int c = threadIdx.x; c < slice / 8; c += blockDim.x) d4[c] = s4[c];
+}
+
+cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, int t,
+                              cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  return launch_k(stage_send_kernel, dim3(M, t), dim3(128), 0, st, src, dst, H, H / t);
+}
+
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;

@@ -910,21 +910,29 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
                        static_cast<cudaStream_t>(stream));
 }
 
-tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
-                     tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
-                     size_t ws_bytes, void* stream) {
-  if (!m || !ids || !h || !logits || !aligned16(h)) return TP_ERR_ARG;
-  if (!m->embed || !m->lm.data || !m->final_norm) return TP_ERR_ARG;
+// Layers [first, first + n) on h; the embedding first when ids is set, the
+// final norm and the LM head after when logits is set.  tp_forward is the
+// single stage covering every layer.
+static tp_status stage_forward(const tp_model* m, int first, int n, const int32_t* ids,
+                               const tp_batch_t* b, tp_bf16* h, tp_bf16* logits,
+                               int64_t ld_logits, int32_t fused, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (!m || !h || !aligned16(h) || first < 0 || n < 0 || first + n > m->cfg.n_layers)
+    return TP_ERR_ARG;
+  if (ids && (first != 0 || !m->embed)) return TP_ERR_ARG;
+  if (logits && (first + n != m->cfg.n_layers || !m->lm.data || !m->final_norm)) return TP_ERR_ARG;
   tp_status s = check_batch(m, b);
   if (s != TP_OK) return s;
-  if (!b->sample_rows || b->n_samples < 1 || ld_logits < m->cfg.vocab) return TP_ERR_ARG;
+  if (logits && (!b->sample_rows || b->n_samples < 1 || ld_logits < m->cfg.vocab)) return TP_ERR_ARG;
   const int M = b->n_tokens;
-  if (!ws_ok(m, std::max(M, b->n_samples), ws, ws_bytes)) return TP_ERR_WORKSPACE;
-  const WsLayout L = ws_layout(m, std::max(M, b->n_samples));
+  const int rows = logits ? std::max(M, b->n_samples) : M;
+  if (!ws_ok(m, rows, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(m, rows);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((s = tp_vocab_embed(m, ids, M, h, stream)) != TP_OK) return s;
-  for (int l = 0; l < m->cfg.n_layers; ++l)
+  if (ids && (s = tp_vocab_embed(m, ids, M, h, stream)) != TP_OK) return s;
+  for (int l = first; l < first + n; ++l)
     if ((s = layer_forward(m, l, b, h, fused, ws, L, st)) != TP_OK) return s;
+  if (!logits) return TP_OK;
   uint16_t* hs = at<uint16_t>(ws, L.hs);
   TP_CHECK_CUDA(launch(m, "rmsnorm_final", st, [&] {
     return launch_rmsnorm(h, m->cfg.hidden, b->sample_rows, m->final_norm, b->n_samples,
@@ -935,6 +943,124 @@ tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
   e.ld_out = ld_logits;
   count_gather(m, b->n_samples);
   return run_column(m, "gemm_lm_head", m->lm, hs, m->cfg.hidden, b->n_samples, EPI_LOGITS, e, ws, L, st);
+}
+
+tp_status tp_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
+                     tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!m || !ids || !logits) return TP_ERR_ARG;
+  return stage_forward(m, 0, m->cfg.n_layers, ids, b, h, logits, ld_logits, fused, ws, ws_bytes,
+                       stream);
+}
+
+tp_status tp_stage_forward(const tp_model* m, int32_t first_layer, int32_t n_layers,
+                           const int32_t* ids, const tp_batch_t* b, tp_bf16* h,
+                           tp_bf16* logits, int64_t ld_logits, int32_t fused, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return stage_forward(m, first_layer, n_layers, ids, b, h, logits, ld_logits, fused, ws,
+                       ws_bytes, stream);
+}
+
+tp_status tp_stage_send(const tp_model* m, const tp_bf16* src, tp_bf16* dst, int32_t M,
+                        void* stream) {
+  if (!m || M < 0) return TP_ERR_ARG;
+  const int H = m->cfg.hidden, t = m->cfg.t;
+  if ((H / t) % 8 || H % t) return TP_ERR_ARG;
+  if (M == 0) return TP_OK;
+  if (!src || !dst || !aligned16(src) || !aligned16(dst)) return TP_ERR_ARG;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(src), b0 = reinterpret_cast<uintptr_t>(dst);
+  const uintptr_t bytes = (uintptr_t)M * H * 2;
+  if (a0 < b0 + bytes && b0 < a0 + bytes) return TP_ERR_ARG;
+  m->stats.stage_sends++;
+  m->stats.stage_send_bytes += (int64_t)bytes;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch(m, "stage_send", st, [&] {
+    return launch_stage_send(src, dst, M, H, t, st);
+  }));
+}
+
+}  // extern "C"
+
+struct tp_graph {
+  const tp_model* m = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  tp_stats_t delta;  // counters of the captured call, added on each replay
+};
+
+namespace {
+template <class F>
+tp_status capture_graph(const tp_model* m, void* stream, tp_graph** out, F&& body) {
+  if (!m || !out || !stream || m->profiling) return TP_ERR_ARG;
+  *out = nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const tp_stats_t before = m->stats;
+  TP_CHECK_CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed));
+  const tp_status s = body();
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(st, &graph);
+  const tp_stats_t after = m->stats;
+  m->stats = before;  // nothing ran yet
+  if (s != TP_OK || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return s != TP_OK ? s : cuda_status(e);
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return cuda_status(ei);
+  tp_graph* g = new tp_graph;
+  g->m = m;
+  g->exec = exec;
+  g->delta.allreduces = after.allreduces - before.allreduces;
+  g->delta.allreduce_payload_bytes = after.allreduce_payload_bytes - before.allreduce_payload_bytes;
+  g->delta.allgathers = after.allgathers - before.allgathers;
+  g->delta.allgather_recv_bytes_per_rank =
+      after.allgather_recv_bytes_per_rank - before.allgather_recv_bytes_per_rank;
+  g->delta.kernel_launches = after.kernel_launches - before.kernel_launches;
+  g->delta.stage_sends = after.stage_sends - before.stage_sends;
+  g->delta.stage_send_bytes = after.stage_send_bytes - before.stage_send_bytes;
+  *out = g;
+  return TP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+tp_status tp_graph_capture_forward(const tp_model* m, const int32_t* ids, const tp_batch_t* b,
+                                   tp_bf16* h, tp_bf16* logits, int64_t ld_logits,
+                                   int32_t fused, void* ws, size_t ws_bytes, void* stream,
+                                   tp_graph** out) {
+  return capture_graph(m, stream, out, [&] {
+    return tp_forward(m, ids, b, h, logits, ld_logits, fused, ws, ws_bytes, stream);
+  });
+}
+
+tp_status tp_graph_capture_layer(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                                 tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
+                                 void* stream, tp_graph** out) {
+  return capture_graph(m, stream, out, [&] {
+    return tp_layer_forward(m, layer, b, h_inout, fused, ws, ws_bytes, stream);
+  });
+}
+
+tp_status tp_graph_launch(tp_graph* g, void* stream) {
+  if (!g || !g->exec) return TP_ERR_ARG;
+  TP_CHECK_CUDA(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)));
+  tp_stats_t& s = g->m->stats;
+  s.allreduces += g->delta.allreduces;
+  s.allreduce_payload_bytes += g->delta.allreduce_payload_bytes;
+  s.allgathers += g->delta.allgathers;
+  s.allgather_recv_bytes_per_rank += g->delta.allgather_recv_bytes_per_rank;
+  s.kernel_launches += g->delta.kernel_launches;
+  s.stage_sends += g->delta.stage_sends;
+  s.stage_send_bytes += g->delta.stage_send_bytes;
+  return TP_OK;
+}
+
+void tp_graph_free(tp_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  delete g;
 }
 
 tp_status tp_get_stats(const tp_model* m, tp_stats_t* out) {

@@ -201,6 +201,71 @@ class TPModel:
         return logits
 
 
+    def stage_forward(self, first_layer: int, n_layers: int, batch: Batch, h: torch.Tensor,
+                      ids: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+                      fused: bool = True, stream=None,
+                      cbatch: Optional[B.tp_batch_t] = None) -> torch.Tensor:
+        M = batch.n_tokens
+        S = int(batch.sample_rows.numel()) if batch.sample_rows is not None else 0
+        self.ensure_workspace(max(M, S), stream)
+        cb = cbatch if cbatch is not None else batch.to_c()
+        B.check(B.tp_stage_forward(self.handle, first_layer, n_layers, _ptr(ids), cb, h.data_ptr(),
+                                   _ptr(logits), self.cfg.vocab, int(fused), *self.ws_args,
+                                   _stream(stream)), "tp_stage_forward")
+        return h
+
+    def stage_send(self, src: torch.Tensor, dst: torch.Tensor, stream=None) -> torch.Tensor:
+        B.check(B.tp_stage_send(self.handle, src.data_ptr(), dst.data_ptr(), src.shape[0],
+                                _stream(stream)), "tp_stage_send")
+        return dst
+
+    def capture_forward(self, ids: torch.Tensor, batch: Batch, h: torch.Tensor,
+                        logits: torch.Tensor, stream, fused: bool = True,
+                        cbatch: Optional[B.tp_batch_t] = None) -> "Graph":
+        """CUDA graph of tp_forward with these buffers (see tp_graph_capture_forward)."""
+        M = batch.n_tokens
+        S = int(batch.sample_rows.numel())
+        self.ensure_workspace(max(M, S), stream)
+        cb = cbatch if cbatch is not None else batch.to_c()
+        st, g = B.tp_graph_capture_forward(self.handle, ids.data_ptr(), cb, h.data_ptr(),
+                                           logits.data_ptr(), self.cfg.vocab, int(fused),
+                                           *self.ws_args, _stream(stream))
+        B.check(st, "tp_graph_capture_forward")
+        return Graph(g, keep=(ids, batch, cb, h, logits, self.ws))
+
+    def capture_layer(self, layer: int, batch: Batch, h: torch.Tensor, stream, fused: bool = True,
+                      cbatch: Optional[B.tp_batch_t] = None) -> "Graph":
+        """CUDA graph of tp_layer_forward with these buffers."""
+        self.ensure_workspace(batch.n_tokens, stream)
+        cb = cbatch if cbatch is not None else batch.to_c()
+        st, g = B.tp_graph_capture_layer(self.handle, layer, cb, h.data_ptr(), int(fused),
+                                         *self.ws_args, _stream(stream))
+        B.check(st, "tp_graph_capture_layer")
+        return Graph(g, keep=(batch, cb, h, self.ws))
+
+
+class Graph:
+    """An executable graph of one captured call; keeps the captured buffers alive."""
+
+    def __init__(self, handle, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def launch(self, stream=None) -> None:
+        B.check(B.tp_graph_launch(self.handle, _stream(stream)), "tp_graph_launch")
+
+    def close(self) -> None:
+        if self.handle:
+            B.tp_graph_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def decode_batch(n_seqs: int, ctx: int, k_cache, v_cache, l_max: Optional[int] = None,
                  with_samples: bool = True) -> Batch:
     dev = "cuda"
