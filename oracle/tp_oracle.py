@@ -155,9 +155,11 @@ def kv_bytes_per_token_per_rank(n_layers: int, n_kv_heads: int, head_dim: int, t
 # ---------------------------------------------------------------------------
 # unsharded layer math
 # ---------------------------------------------------------------------------
-def linear(x: Array, w: Array) -> Array:
-    """Y = X W^T for a weight stored [out, in] (the pages' Y = XW)."""
-    return x @ w.T
+def linear(x: Array, w: Array, b: Optional[Array] = None) -> Array:
+    """Y = X W^T (+ b) for a weight stored [out, in] (the pages' Y = XW) and
+    an optional bias over the output features."""
+    y = x @ w.T
+    return y if b is None else y + b
 
 
 def rmsnorm(x: Array, w: Array, eps: float) -> Array:
@@ -243,6 +245,15 @@ class LayerWeights:
     wg: Array
     wu: Array
     wd: Array
+    # optional biases over each projection's output features (Qwen2.5-style
+    # models carry bq, bk, bv); None = no bias
+    bq: Optional[Array] = None
+    bk: Optional[Array] = None
+    bv: Optional[Array] = None
+    bo: Optional[Array] = None
+    bg: Optional[Array] = None
+    bu: Optional[Array] = None
+    bd: Optional[Array] = None
 
 
 @dataclass
@@ -270,9 +281,9 @@ def layer_forward(h: Array, W: LayerWeights, kcache: dict, vcache: dict, batch: 
     T = h.shape[0]
     nh, nkv, d = dims.n_heads, dims.n_kv_heads, dims.head_dim
     u = rb(rmsnorm(h, W.attn_norm, dims.rms_eps))
-    q = linear(u, W.wq).reshape(T, nh, d)
-    k = linear(u, W.wk).reshape(T, nkv, d)
-    v = linear(u, W.wv).reshape(T, nkv, d)
+    q = linear(u, W.wq, W.bq).reshape(T, nh, d)
+    k = linear(u, W.wk, W.bk).reshape(T, nkv, d)
+    v = linear(u, W.wv, W.bv).reshape(T, nkv, d)
     q = rb(rope(q, batch.pos, dims.rope_theta))
     k = rb(rope(k, batch.pos, dims.rope_theta))
     v = rb(v)
@@ -285,10 +296,10 @@ def layer_forward(h: Array, W: LayerWeights, kcache: dict, vcache: dict, batch: 
         b, p = int(batch.seq[i]), int(batch.pos[i])
         o[i] = gqa_attend_token(q[i], kcache[b], vcache[b], p)
     o = rb(o.reshape(T, nh * d))
-    h = rb(h + linear(o, W.wo))
+    h = rb(h + linear(o, W.wo, W.bo))
     u2 = rb(rmsnorm(h, W.mlp_norm, dims.rms_eps))
-    a = rb(silu(linear(u2, W.wg)) * linear(u2, W.wu))
-    return rb(h + linear(a, W.wd))
+    a = rb(silu(linear(u2, W.wg, W.bg)) * linear(u2, W.wu, W.bu))
+    return rb(h + linear(a, W.wd, W.bd))
 
 
 def embed(E: Array, ids: Array) -> Array:
@@ -316,6 +327,33 @@ def shard_qkv(W: LayerWeights, dims: Dims, p: Plan) -> List[Array]:
         vrows = np.concatenate([W.wv[g * d:(g + 1) * d] for g in kvh])
         out.append(np.concatenate([qrows, krows, vrows]))
     return out
+
+
+def shard_qkv_bias(W: LayerWeights, dims: Dims, p: Plan) -> List[Array]:
+    """Column-parallel bias: split with its weight along the output features
+    ("第 9 章", §3.2: weights and their biases are cut along the output
+    dimension), so rank r holds the bias entries of exactly its own q/k/v
+    rows (copies for replicated KV heads)."""
+    d = dims.head_dim
+    zq = np.zeros(dims.n_heads * d) if W.bq is None else W.bq
+    zk = np.zeros(dims.n_kv_heads * d) if W.bk is None else W.bk
+    zv = np.zeros(dims.n_kv_heads * d) if W.bv is None else W.bv
+    out = []
+    for r in range(p.t):
+        kvh = kv_heads_of_rank(p, dims.n_kv_heads, r)
+        out.append(np.concatenate([zq[j * d:(j + 1) * d] for j in q_heads_of_rank(p, r)] +
+                                  [zk[g * d:(g + 1) * d] for g in kvh] +
+                                  [zv[g * d:(g + 1) * d] for g in kvh]))
+    return out
+
+
+def shard_gate_up_bias(W: LayerWeights, p: Plan) -> List[Array]:
+    """The gate and up biases cut like their rows."""
+    n = p.inter_per_rank
+    I = p.inter_per_rank * p.t
+    zg = np.zeros(I) if W.bg is None else W.bg
+    zu = np.zeros(I) if W.bu is None else W.bu
+    return [np.concatenate([zg[r * n:(r + 1) * n], zu[r * n:(r + 1) * n]]) for r in range(p.t)]
 
 
 def shard_gate_up(W: LayerWeights, p: Plan) -> List[Array]:
@@ -379,25 +417,36 @@ def sharded_lm_head(x: Array, L_shards: List[Array], vocab: int, rb: Callable = 
 
 def sharded_layer_forward(h: Array, W: LayerWeights, kcopies: List[dict], vcopies: List[dict],
                           batch: Batch, dims: Dims, p: Plan, rb: Callable = round_bf16,
-                          skip_allreduce: bool = False) -> Array:
+                          skip_allreduce: bool = False, bias_on_every_rank: bool = False) -> Array:
     """The same layer computed as t ranks: column shards with no
     communication, per-rank attention over the rank's own heads and cache,
     row-parallel partials summed by an all-reduce (① after o_proj, ② after
     down_proj).  kcopies[c][b]: cache copy c of sequence b, [kv_r, L_max, d].
 
     ``skip_allreduce`` keeps only rank 0's partial (the "missing collective"
-    fault of the pages' debugging checklist)."""
+    fault of the pages' debugging checklist).  A row-parallel bias belongs to
+    the whole output, so it is added once, after the all-reduce;
+    ``bias_on_every_rank`` instead adds it to every rank's partial (the t-fold
+    bias a misplaced add would produce), for the tests."""
     T = h.shape[0]
     d = dims.head_dim
     nq = p.q_heads_per_rank
     group = dims.n_heads // dims.n_kv_heads
     reduce = (lambda parts: parts[0]) if skip_allreduce else all_reduce_sum
 
+    def row_bias(partials, b):
+        if b is None:
+            return reduce(partials)
+        if bias_on_every_rank:
+            return reduce([y + b for y in partials])
+        return reduce(partials) + b
+
     u = rb(rmsnorm(h, W.attn_norm, dims.rms_eps))       # replicated on every rank
     qkv_sh = shard_qkv(W, dims, p)
+    qkv_b = shard_qkv_bias(W, dims, p)
     o_parts = []
     for r in range(p.t):
-        y = linear(u, qkv_sh[r])                          # Y_r = X A_r
+        y = linear(u, qkv_sh[r], qkv_b[r])                # Y_r = X A_r + b_r
         kvh = kv_heads_of_rank(p, dims.n_kv_heads, r)
         nkv = len(kvh)
         q = rb(rope(y[:, : nq * d].reshape(T, nq, d), batch.pos, dims.rope_theta))
@@ -419,18 +468,19 @@ def sharded_layer_forward(h: Array, W: LayerWeights, kcopies: List[dict], vcopie
                 gl = kvh.index(j // group)
                 o[i, jl] = attend(q[i, jl], kcopies[c][b][gl, : pos + 1], vcopies[c][b][gl, : pos + 1])
         partials.append(linear(rb(o.reshape(T, nq * d)), Wo_sh[r]))
-    h = rb(h + reduce(partials))
+    h = rb(h + row_bias(partials, W.bo))
 
     u2 = rb(rmsnorm(h, W.mlp_norm, dims.rms_eps))
     gu_sh = shard_gate_up(W, p)
+    gu_b = shard_gate_up_bias(W, p)
     Wd_sh = shard_rows_by_input(W.wd, p.t)
     n = p.inter_per_rank
     partials = []
     for r in range(p.t):
-        y = linear(u2, gu_sh[r])
+        y = linear(u2, gu_sh[r], gu_b[r])
         a = rb(silu(y[:, :n]) * y[:, n:])
         partials.append(linear(a, Wd_sh[r]))
-    return rb(h + reduce(partials))
+    return rb(h + row_bias(partials, W.bd))
 
 
 def split_cache_copies(kcache: dict, dims: Dims, p: Plan) -> List[dict]:

@@ -352,3 +352,97 @@ def test_batch_sample_rows_are_last_tokens():
     b = O.Batch.prefill(3, 4)
     assert list(b.sample_rows()) == [3, 7, 11]
     assert list(O.Batch.decode(5, 9).sample_rows()) == [0, 1, 2, 3, 4]
+
+
+# ---------------------------------------------------------------------------
+# projection biases ("第 9 章", §3.2: a weight and its bias are cut along the
+# output dimension; the bias of a row-parallel output is added once)
+# ---------------------------------------------------------------------------
+def _with_biases(dims, W, seed=21, sigma=0.5):
+    d, H, I = dims.head_dim, dims.hidden, dims.intermediate
+    W.bq = synth.normal_f64(seed, 1, (dims.n_heads * d,), sigma)
+    W.bk = synth.normal_f64(seed, 2, (dims.n_kv_heads * d,), sigma)
+    W.bv = synth.normal_f64(seed, 3, (dims.n_kv_heads * d,), sigma)
+    W.bo = synth.normal_f64(seed, 4, (H,), sigma)
+    W.bg = synth.normal_f64(seed, 5, (I,), sigma)
+    W.bu = synth.normal_f64(seed, 6, (I,), sigma)
+    W.bd = synth.normal_f64(seed, 7, (H,), sigma)
+    return W
+
+
+def test_linear_bias_closed_forms():
+    x = np.array([[1.0, 2.0], [3.0, -1.0]])
+    w = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    b = np.array([0.5, -0.25, 10.0])
+    assert np.array_equal(O.linear(x, w, b), np.array([[1.5, 1.75, 13.0], [3.5, -1.25, 12.0]]))
+    assert np.array_equal(O.linear(x, np.zeros((3, 2)), b), np.tile(b, (2, 1)))
+
+
+def test_row_parallel_biases_enter_once():
+    # with o_proj and down_proj weights zero the layer reduces to
+    # h -> round(round(h + bo) + bd), whatever the attention and MLP compute
+    dims, W = _tiny(4, 2)
+    W = _with_biases(dims, W)
+    W.wo[:] = 0.0
+    W.wd[:] = 0.0
+    batch = O.Batch.decode(2, 5)
+    h = O.round_bf16(synth.normal_f64(9, 13, (2, dims.hidden), 1.0))
+    kc, vc = _caches(2, 2, 5, dims.head_dim)
+    want = O.round_bf16(O.round_bf16(h + W.bo) + W.bd)
+    assert np.array_equal(O.layer_forward(h, W, _copy(kc), _copy(vc), batch, dims), want)
+    for t in (2, 4):
+        p = O.plan(4, 2, dims.intermediate, dims.vocab, t)
+        got = O.sharded_layer_forward(h, W, O.split_cache_copies(_copy(kc), dims, p),
+                                      O.split_cache_copies(_copy(vc), dims, p), batch, dims, p)
+        assert np.array_equal(got, want)
+        bad = O.sharded_layer_forward(h, W, O.split_cache_copies(_copy(kc), dims, p),
+                                      O.split_cache_copies(_copy(vc), dims, p), batch, dims, p,
+                                      rb=O.no_round, bias_on_every_rank=True)
+        assert np.allclose(bad - h, t * (W.bo + W.bd), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("n_heads,n_kv,t", [(4, 4, 2), (4, 2, 4), (4, 1, 2), (8, 2, 8), (6, 3, 3)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_sharded_layer_with_biases_equals_unsharded(n_heads, n_kv, t, mode):
+    dims, W = _tiny(n_heads, n_kv)
+    W = _with_biases(dims, W)
+    batch = O.Batch.decode(3, 7) if mode == "decode" else O.Batch.prefill(2, 5)
+    n_seqs = 3 if mode == "decode" else 2
+    L = 7 if mode == "decode" else 5
+    T = len(batch.seq)
+    h = synth.normal_f64(9, 9, (T, dims.hidden), 1.0)
+    kc, vc = _caches(n_seqs, n_kv, L, dims.head_dim)
+    p = O.plan(n_heads, n_kv, dims.intermediate, dims.vocab, t)
+    ref = O.layer_forward(h, W, _copy(kc), _copy(vc), batch, dims, rb=O.no_round)
+    got = O.sharded_layer_forward(h, W, O.split_cache_copies(_copy(kc), dims, p),
+                                  O.split_cache_copies(_copy(vc), dims, p), batch, dims, p,
+                                  rb=O.no_round)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 1e-12
+    # and the biases matter at this scale
+    W0 = _tiny(n_heads, n_kv)[1]
+    nob = O.layer_forward(h, W0, _copy(kc), _copy(vc), batch, dims, rb=O.no_round)
+    assert np.max(np.abs(nob - ref)) / np.max(np.abs(ref)) > 0.05
+
+
+def test_qk_bias_is_added_before_rope():
+    # head_dim 2 (one rotation pair, angle = position x 1 rad), one head, one
+    # KV head, zero q/k weights: q = R(1) bq and k_new = R(1) bk at position 1,
+    # against a cached key k0 at position 0.  Attention weights of the two
+    # keys are softmax([q.k0, q.k_new] / sqrt(2)); with bq = (1, 0), bk = (0, 0),
+    # k0 = (1, 0): q.k0 = cos 1 (bias rotated) rather than 1 (bias added after
+    # the rotation); the output is the weighted mix of v0 and v_new = bv.
+    H = 4
+    dims = O.Dims(H, 1, 1, 2, 4, 10)
+    z = lambda *s: np.zeros(s)
+    W = O.LayerWeights(attn_norm=np.ones(H), wq=z(2, H), wk=z(2, H), wv=z(2, H),
+                       wo=np.eye(H, 2), mlp_norm=np.ones(H), wg=z(4, H), wu=z(4, H), wd=z(H, 4),
+                       bq=np.array([1.0, 0.0]), bk=np.zeros(2), bv=np.array([0.0, 3.0]))
+    batch = O.Batch.decode(1, 2)               # the new token sits at position 1
+    kc = {0: np.array([[[1.0, 0.0], [0.0, 0.0]]])}
+    vc = {0: np.array([[[2.0, 0.0], [0.0, 0.0]]])}
+    h = np.zeros((1, H))
+    out = O.layer_forward(h, W, kc, vc, batch, dims, rb=O.no_round)
+    s0, s1 = np.cos(1.0) / np.sqrt(2.0), 0.0
+    a0 = np.exp(s0) / (np.exp(s0) + np.exp(s1))
+    want = np.array([2.0 * a0, 3.0 * (1 - a0), 0.0, 0.0])
+    assert np.allclose(out[0], want, rtol=1e-12, atol=1e-12)
