@@ -96,9 +96,17 @@ tp_status tp_config(tp_config_t* c);
 
 /* Unsharded weights of one decoder layer (device pointers, bf16).
  * attn_norm, mlp_norm [H]; wq [n_heads*d, H]; wk, wv [n_kv*d, H];
- * wo [H, n_heads*d]; wg, wu [I, H]; wd [H, I]. */
+ * wo [H, n_heads*d]; wg, wu [I, H]; wd [H, I].
+ * Optional biases over each projection's output features (NULL = none;
+ * Qwen2.5-style models carry bq, bk, bv): bq [n_heads*d]; bk, bv [n_kv*d];
+ * bo [H]; bg, bu [I]; bd [H].  A column-parallel bias is cut with its weight
+ * rows (P1 §3.2 切分: weights and their biases split along the output
+ * dimension), so rank r adds the entries of its own rows; the bias of a
+ * row-parallel output (bo, bd) belongs to the whole reduced output and is
+ * added once, after the reduction, before the residual. */
 typedef struct {
   const tp_bf16 *attn_norm, *wq, *wk, *wv, *wo, *mlp_norm, *wg, *wu, *wd;
+  const tp_bf16 *bq, *bk, *bv, *bo, *bg, *bu, *bd;
 } tp_layer_weights_t;
 
 /* embed, lm_head [vocab, H]; final_norm [H]: may all be NULL for a model used
@@ -147,7 +155,8 @@ enum { TP_QKV = 0, TP_GATE_UP = 1, TP_O = 2, TP_DOWN = 3 };
  *           for TP_QKV (its Q heads, then K heads, then V heads) and
  *           N_r = 2 I/t for TP_GATE_UP (gate slice, then up slice).
  *           y_rank_stride >= M*N_r.
- * Plain GEMM output: no RoPE, no activation. */
+ * Plain GEMM output plus the rank's slice of the layer's bias when the model
+ * has one (bq/bk/bv or bg/bu): no RoPE, no activation. */
 tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
                            int32_t M, tp_bf16* y, int64_t y_rank_stride, void* ws,
                            size_t ws_bytes, void* stream);
@@ -158,6 +167,8 @@ tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, cons
  *   x        : rank r's input shard at x + r*x_rank_stride, [M, K_r] with row
  *              stride ldx (K_r = n_heads*d/t for TP_O, I/t for TP_DOWN)
  *   residual : [M, H] or NULL; added once, in fp32, before the rounding
+ *   bias     : the layer's bo / bd, when the model has one, is added once to
+ *              the reduced sum (not per rank), in fp32, before the residual
  *   y        : [M, H] bf16; may alias `residual`
  *   fused    : 1 = one kernel; the t partials are accumulated in fp32 in
  *              rank order 0..t-1 and rounded once to bf16 in its epilogue.

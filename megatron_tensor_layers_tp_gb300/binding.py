@@ -34,7 +34,7 @@ class tp_config_t(Structure):
 
 class tp_layer_weights_t(Structure):
     _fields_ = [(n, c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu",
-                                        "wd")]
+                                        "wd", "bq", "bk", "bv", "bo", "bg", "bu", "bd")]
 
 
 class tp_weights_t(Structure):

@@ -76,7 +76,13 @@ struct EpiIn {
   int pos[16];
   int seq[16];
   float2 cs[16];
+  float b[16];  // output bias: one value per row (decode) or per column (prefill)
 };
+
+// Epilogues that add the GEMM's output bias (the unfused row-parallel
+// partials leave it to the rank reduction; the LM head has none).
+template <int EPI>
+constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || EPI == EPI_RESID;
 
 template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int brow0,
@@ -84,6 +90,18 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
   const EpiArgs& e = a.e;
   const int f = arow;
   const bool fval = f < a.a_rows_valid;
+  if constexpr (kEpiBias<EPI>) {
+    if (e.bias) {
+      const uint16_t* bg = e.bias + (int64_t)g * e.bias_group_stride;
+      if constexpr (SWAP) {
+        in.b[0] = fval ? bf16_to_f(bg[f]) : 0.f;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          in.b[j] = brow0 + j < a.b_rows_valid ? bf16_to_f(bg[brow0 + j]) : 0.f;
+      }
+    }
+  }
   if constexpr (SWAP && EPI == EPI_RESID) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -137,6 +155,12 @@ template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
                                           float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
+  if constexpr (kEpiBias<EPI>) {
+    if (e.bias) {  // before RoPE / SiLU pairing and the residual
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] += SWAP ? in.b[0] : in.b[j];
+    }
+  }
   if constexpr (SWAP) {
     const int f = arow;
     const bool fval = f < a.a_rows_valid;

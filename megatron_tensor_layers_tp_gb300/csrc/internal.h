@@ -46,6 +46,10 @@ struct EpiArgs {
   // EPI_LOGITS
   int vocab;
   int vocab_per_rank;
+  // optional bias over the output features (PLAIN, QKV, SILU, RESID): the
+  // value of output row f of rank g is bias[g * bias_group_stride + f]
+  const uint16_t* bias;
+  int64_t bias_group_stride;
 };
 
 struct GemmArgs {
@@ -154,7 +158,8 @@ cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, i
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
                            int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st);
 cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int t, int M, int H,
-                                const uint16_t* residual, uint16_t* y, cudaStream_t st);
+                                const uint16_t* bias, const uint16_t* residual, uint16_t* y,
+                                cudaStream_t st);
 cudaError_t launch_rope_table(float2* table, int max_pos, int head_dim, double theta,
                               cudaStream_t st);
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,

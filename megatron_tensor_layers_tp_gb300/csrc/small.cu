@@ -121,8 +121,8 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, 
 // all-reduce of a row-parallel layer is a sum).  P_r: [M, H] fp32 partials.
 // ---------------------------------------------------------------------------
 __global__ void reduce_ranks_kernel(const float4* __restrict__ P, int64_t rank_stride4, int t,
-                                    int64_t n4, int H4, const uint2* __restrict__ residual,
-                                    uint2* __restrict__ y) {
+                                    int64_t n4, int H4, const uint2* __restrict__ bias,
+                                    const uint2* __restrict__ residual, uint2* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -131,6 +131,13 @@ __global__ void reduce_ranks_kernel(const float4* __restrict__ P, int64_t rank_s
     for (int r = 1; r < t; ++r) {
       const float4 p = P[r * rank_stride4 + i];
       acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    if (bias) {  // the output's bias, once, after the rank sum
+      const uint2 bv = bias[i % H4];
+      acc.x += __uint_as_float(bv.x << 16);
+      acc.y += __uint_as_float(bv.x & 0xFFFF0000u);
+      acc.z += __uint_as_float(bv.y << 16);
+      acc.w += __uint_as_float(bv.y & 0xFFFF0000u);
     }
     if (residual) {
       const uint2 rv = residual[i];
@@ -144,14 +151,16 @@ __global__ void reduce_ranks_kernel(const float4* __restrict__ P, int64_t rank_s
 }
 
 cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int t, int M, int H,
-                                const uint16_t* residual, uint16_t* y, cudaStream_t st) {
+                                const uint16_t* bias, const uint16_t* residual, uint16_t* y,
+                                cudaStream_t st) {
   const int64_t n4 = (int64_t)M * H / 4;
   if (n4 == 0) return cudaSuccess;
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
   return launch_k(reduce_ranks_kernel, dim3(blocks), dim3(256), 0, st,
                   reinterpret_cast<const float4*>(partials), rank_stride / 4, t, n4, H / 4,
-                  reinterpret_cast<const uint2*>(residual), reinterpret_cast<uint2*>(y));
+                  reinterpret_cast<const uint2*>(bias), reinterpret_cast<const uint2*>(residual),
+                  reinterpret_cast<uint2*>(y));
 }
 
 // ---------------------------------------------------------------------------

@@ -18,6 +18,7 @@ using namespace tpk;
 
 struct ShardedLinear {
   uint16_t* data = nullptr;  // [t][rows][cols]
+  uint16_t* bias = nullptr;  // optional: [t][rows] (column-parallel) or [rows] (row-parallel)
   int rows = 0, cols = 0;    // per rank
   CUtensorMap tm_a;          // box (64, 128, 1): weight on the MMA M side (decode)
   CUtensorMap tm_b;          // box (64, 256, 1): weight on the MMA N side (prefill)
@@ -319,6 +320,8 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
   a.e = e;
+  a.e.bias = W.bias;  // rank g's rows carry their own bias entries
+  a.e.bias_group_stride = W.rows;
   return cuda_status(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
 }
 
@@ -373,6 +376,8 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
     a.e.ld_out = H;
     a.e.residual = residual;
     a.e.ld_res = H;
+    a.e.bias = W.bias;  // once: the ranks are already summed in the accumulator
+    a.e.bias_group_stride = 0;
     epi = EPI_RESID;
   } else {
     a.n_groups = t;
@@ -388,7 +393,7 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
   TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
   if (!fused) {
     TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {
-      return launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, residual, y, st);
+      return launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, W.bias, residual, y, st);
     }));
   }
   m->stats.allreduces++;
@@ -651,6 +656,40 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
       uint16_t* gbase = Ls.gate_up.data + (size_t)r * 2 * Ipr * H;
       if (launch_copy_rows(gbase, 2 * H, Wl.wg, H, dg, Ipr, H, st) != cudaSuccess ||
           launch_copy_rows(gbase + H, 2 * H, Wl.wu, H, dg, Ipr, H, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+      // biases follow their rows (one element per row; a missing part is zero)
+      if (Wl.bq || Wl.bk || Wl.bv) {
+        if (!Ls.qkv.bias && (s = dev_alloc(m, &Ls.qkv.bias, (size_t)t * nqkv * 2)) != TP_OK)
+          return fail(s);
+        int32_t *nq_, *nk_;
+        std::vector<int32_t> zq(nq * d, -1), zk(kvr * d, -1);
+        if ((s = up.upload(zq, &nq_, st)) != TP_OK || (s = up.upload(zk, &nk_, st)) != TP_OK)
+          return fail(s);
+        uint16_t* bb = Ls.qkv.bias + (size_t)r * nqkv;
+        if (launch_copy_rows(bb, 1, Wl.bq, 1, Wl.bq ? dq : nq_, nq * d, 1, st) != cudaSuccess ||
+            launch_copy_rows(bb + nq * d, 1, Wl.bk, 1, Wl.bk ? dk : nk_, kvr * d, 1, st) !=
+                cudaSuccess ||
+            launch_copy_rows(bb + (nq + kvr) * d, 1, Wl.bv, 1, Wl.bv ? dv : nk_, kvr * d, 1, st) !=
+                cudaSuccess)
+          return fail(TP_ERR_CUDA);
+      }
+      if (Wl.bg || Wl.bu) {
+        if (!Ls.gate_up.bias && (s = dev_alloc(m, &Ls.gate_up.bias, (size_t)t * 2 * Ipr * 2)) != TP_OK)
+          return fail(s);
+        int32_t* ng_;
+        std::vector<int32_t> zg(Ipr, -1);
+        if ((s = up.upload(zg, &ng_, st)) != TP_OK) return fail(s);
+        uint16_t* gb = Ls.gate_up.bias + (size_t)r * 2 * Ipr;
+        if (launch_copy_rows(gb, 2, Wl.bg, 1, Wl.bg ? dg : ng_, Ipr, 1, st) != cudaSuccess ||
+            launch_copy_rows(gb + 1, 2, Wl.bu, 1, Wl.bu ? dg : ng_, Ipr, 1, st) != cudaSuccess)
+          return fail(TP_ERR_CUDA);
+      }
+    }
+    // row-parallel biases: whole [H] vectors, added once after the reduction
+    for (auto [src, dst] : {std::make_pair(Wl.bo, &Ls.o.bias), std::make_pair(Wl.bd, &Ls.down.bias)}) {
+      if (!src) continue;
+      if ((s = dev_alloc(m, dst, (size_t)H * 2)) != TP_OK) return fail(s);
+      if (cudaMemcpyAsync(*dst, src, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return fail(TP_ERR_CUDA);
     }
     // row-parallel shards: columns [r K_r, (r+1) K_r) of wo / wd

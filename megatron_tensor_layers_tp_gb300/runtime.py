@@ -69,6 +69,7 @@ class TPModel:
     """Owns one tp_model (the t ranks' shards) plus a workspace."""
 
     LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wg", "wu", "wd")
+    BIAS_KEYS = ("bq", "bk", "bv", "bo", "bg", "bu", "bd")
 
     def __init__(self, cfg: B.tp_config_t, layers: Sequence[Dict[str, torch.Tensor]],
                  embed: Optional[torch.Tensor] = None, final_norm: Optional[torch.Tensor] = None,
@@ -81,6 +82,11 @@ class TPModel:
                 t = L[k]
                 assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), k
                 setattr(arr[i], k, t.data_ptr())
+            for k in self.BIAS_KEYS:  # optional
+                t = L.get(k)
+                if t is not None:
+                    assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), k
+                    setattr(arr[i], k, t.data_ptr())
         w = B.tp_weights_t()
         w.embed, w.final_norm, w.lm_head = _ptr(embed), _ptr(final_norm), _ptr(lm_head)
         w.layers = ctypes.cast(arr, ctypes.POINTER(B.tp_layer_weights_t))

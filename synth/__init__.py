@@ -92,7 +92,9 @@ _KINDS = {
     "embed": 1, "lm_head": 2, "final_norm": 3, "attn_norm": 4, "mlp_norm": 5,
     "wq": 6, "wk": 7, "wv": 8, "wo": 9, "wg": 10, "wu": 11, "wd": 12,
     "k_cache": 13, "v_cache": 14, "hidden": 15, "ids": 16, "x": 17,
+    "bq": 18, "bk": 19, "bv": 20, "bo": 21, "bg": 22, "bu": 23, "bd": 24,
 }
+BIAS_KINDS = ("bq", "bk", "bv", "bo", "bg", "bu", "bd")
 
 
 def tensor_id(kind: str, layer: int = 0) -> int:
@@ -180,6 +182,8 @@ class Workload:
     sigma_kv: float = 1.0
     sigma_h: float = 1.0
     norm_weight_sigma: float = 0.0   # 0: norm weights are exactly 1
+    bias: bool = False               # projections carry biases (BIAS_KINDS)
+    sigma_b: float = 0.5
     rms_eps: float = 1e-5
     rope_theta: float = 10000.0
 
@@ -221,6 +225,15 @@ def weight_shapes(w: Workload, layer: int) -> dict:
     }
 
 
+def bias_shapes(w: Workload) -> dict:
+    """Shapes of the projection biases (empty when the workload has none)."""
+    if not w.bias:
+        return {}
+    H, d = w.hidden, w.head_dim
+    return {"bq": (w.n_heads * d,), "bk": (w.n_kv_heads * d,), "bv": (w.n_kv_heads * d,),
+            "bo": (H,), "bg": (w.intermediate,), "bu": (w.intermediate,), "bd": (H,)}
+
+
 def sigma_for(w: Workload, kind: str) -> float:
     if kind in ("attn_norm", "mlp_norm", "final_norm"):
         return w.norm_weight_sigma
@@ -228,6 +241,8 @@ def sigma_for(w: Workload, kind: str) -> float:
         return w.sigma_kv
     if kind in ("hidden", "x"):
         return w.sigma_h
+    if kind in BIAS_KINDS:
+        return w.sigma_b
     return w.sigma_w
 
 

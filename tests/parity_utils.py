@@ -37,7 +37,9 @@ def oracle_dims(w: Workload):
 def oracle_layer(w: Workload, layer: int):
     import oracle as O
     shapes = synth.weight_shapes(w, layer)
-    return O.LayerWeights(**{k: synth.host_weight(w, k, layer, shapes[k]) for k in LAYER_KINDS})
+    shapes.update(synth.bias_shapes(w))
+    return O.LayerWeights(**{k: synth.host_weight(w, k, layer, shapes[k])
+                             for k in (*LAYER_KINDS, *synth.bias_shapes(w))})
 
 
 def oracle_caches(w: Workload, layer: int, seqs: Sequence[int]):
@@ -64,7 +66,8 @@ def device_weight(w: Workload, kind: str, layer: int, shape):
 
 def device_layer(w: Workload, layer: int) -> Dict[str, "torch.Tensor"]:
     shapes = synth.weight_shapes(w, layer)
-    return {k: device_weight(w, k, layer, shapes[k]) for k in LAYER_KINDS}
+    shapes.update(synth.bias_shapes(w))
+    return {k: device_weight(w, k, layer, shapes[k]) for k in (*LAYER_KINDS, *synth.bias_shapes(w))}
 
 
 def fill_device_kv(model, w: Workload, cache, kind: str, layer: int) -> None:
