@@ -68,13 +68,13 @@ __device__ __forceinline__ int plain_col(const EpiArgs& e, int f) {
 
 // Inputs of the epilogues (residual values; token positions, sequences and
 // RoPE factors), fetched by epi_load ahead of the arithmetic so their latency
-// overlaps the other loads of a fix-up.  In the decode orientation positions
-// and sequences come from the CTA's shared-memory copy (tok: positions of
-// tokens 0..kSwapMaxTokens-1, then their sequences).
+// overlaps the other loads of a fix-up.  In the decode orientation the
+// tokens' positions come from the CTA's shared-memory copy (tok: positions of
+// tokens 0..kSwapMaxTokens-1, their sequences, then each token's part of a
+// K/V cache index as int64).
 struct EpiIn {
   float r[16];
   int pos[16];
-  int seq[16];
   float2 cs[16];
   float b[16];  // output bias: one value per row (decode) or per column (prefill)
 };
@@ -83,6 +83,11 @@ struct EpiIn {
 // partials leave it to the rank reduction; the LM head has none).
 template <int EPI>
 constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || EPI == EPI_RESID;
+// Multi-chunk epilogues fetch the next chunk's inputs before storing the
+// current one, except qkv, whose inputs (positions, RoPE factors) would not
+// fit in registers twice next to the fix-up's pieces.
+template <int EPI>
+constexpr bool kEpiAhead = EPI != EPI_QKV;
 
 template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int brow0,
@@ -116,9 +121,7 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int m = brow0 + j;
-      const bool ok = fval && m < e.M;
-      in.pos[j] = ok ? tok[m] : -1;
-      in.seq[j] = (ok && kind != 0) ? tok[kSwapMaxTokens + m] : 0;
+      in.pos[j] = (fval && m < e.M) ? tok[m] : -1;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -153,7 +156,7 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
 
 template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
-                                          float (&v)[16], const EpiIn& in) {
+                                          const int* tok, float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
   if constexpr (kEpiBias<EPI>) {
     if (e.bias) {  // before RoPE / SiLU pairing and the residual
@@ -207,7 +210,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
         const int m = brow0 + j;
         if (fval && !(f & 1) && m < e.M) {
           const float gt = v[j], up = partner;
-          out[(int64_t)m * e.ld_out + col] = f_to_bf16(gt / (1.f + expf(-gt)) * up);
+          out[(int64_t)m * e.ld_out + col] = f_to_bf16(__fdividef(gt, 1.f + __expf(-gt)) * up);
         }
       }
     } else if constexpr (EPI == EPI_QKV) {
@@ -220,6 +223,10 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       const bool primary = (g % e.kv_replicas) == 0;
       const int copy = g / e.kv_replicas;
       uint16_t* qout = static_cast<uint16_t*>(e.out);
+      // this thread's (copy, KV head, feature) part of a cache index; the
+      // token's part ((seq * kv_r) * l_max + pos) * d is staged in shared memory
+      uint16_t* cache_row = (kind == 1 ? e.k_cache : e.v_cache) + copy * e.kv_copy_stride +
+                            (int64_t)head * e.l_max * d + feat;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
@@ -236,11 +243,8 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
           qout[(int64_t)m * e.ld_out + (int64_t)(g * e.q_heads_per_rank + head) * d + feat] =
               f_to_bf16(val);
         } else if (primary) {
-          const int seq = in.seq[j];
-          uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
-          const int64_t idx = copy * e.kv_copy_stride +
-                              (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d + feat;
-          cache[idx] = f_to_bf16(val);
+          cache_row[reinterpret_cast<const int64_t*>(tok + 2 * kSwapMaxTokens)[m]] =
+              f_to_bf16(val);
         }
       }
     }
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* tok = reinterpret_cast<int*>(last_flag + 3);  // decode: token positions, then sequences
+  int* tok = reinterpret_cast<int*>(last_flag + 3);  // decode: positions, sequences, cache offsets
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -589,8 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // every tile of the decode orientation covers tokens 0..M-1
       if (et < kSwapMaxTokens) {
         const bool ok = et < a.e.M;
-        tok[et] = ok ? a.e.positions[et] : -1;
-        tok[kSwapMaxTokens + et] = ok ? a.e.token_seq[et] : 0;
+        const int pos = ok ? a.e.positions[et] : -1;
+        const int seq = ok ? a.e.token_seq[et] : 0;
+        tok[et] = pos;
+        tok[kSwapMaxTokens + et] = seq;
+        reinterpret_cast<int64_t*>(tok + 2 * kSwapMaxTokens)[et] =
+            ((int64_t)seq * a.e.kv_heads_per_rank * a.e.l_max + pos) * a.e.head_dim;
       }
       bar_sync(1, 128);
     }
@@ -661,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
             tmem_ld16(taddr + c0, v);
             tmem_ld_wait();
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
           }
         } else {
           // inputs of chunk c0 + 16 are fetched before chunk c0 is stored
@@ -672,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             float v[16];
             tmem_ld16(taddr + c0, v);
             tmem_ld_wait();
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, cur);
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, cur);
             cur = nxt;
           }
         }
@@ -723,10 +731,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
           };
           load_batch(0, 0);
+          EpiIn in;  // inputs of the current chunk; those of the next are fetched ahead
+          if (use_pre) in = pre;
+          else epi_load<SWAP, EPI>(a, g, arow, brow, tok, in);
           for (int c0 = 0; c0 < BN; c0 += 16) {
-            EpiIn in;
-            if (use_pre && c0 == 0) in = pre;
-            else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
+            EpiIn nxt;
+            if constexpr (kEpiAhead<EPI>)
+              if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -740,7 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               if (s0 + 4 < nseg) load_batch(c0, s0 + 4);
               else if (c0 + 16 < BN) load_batch(c0 + 16, 0);
             }
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
+            if constexpr (kEpiAhead<EPI>) in = nxt;
+            else if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, in);
           }
           if (threadIdx.x == 64) a.tickets[sg.tile] = 0;
         }
@@ -763,10 +776,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t red_s = smem_u32(smem);
       // rank r sums and stores chunks r, r + s, ...; the pieces are added in
       // K order (rank 0 first), up to 4 remote loads in flight together
-      for (int c0 = rank * 16; c0 < BN; c0 += a.cluster_split * 16) {
-        EpiIn in;
-        if (pre_ok && c0 == rank * 16) in = pre;
-        else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
+      const int cstep = a.cluster_split * 16;
+      EpiIn in;  // inputs of the current chunk; those of the next are fetched ahead
+      if (pre_ok) in = pre;
+      else if (rank * 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + rank * 16, tok, in);
+      for (int c0 = rank * 16; c0 < BN; c0 += cstep) {
+        EpiIn nxt;
+        if constexpr (kEpiAhead<EPI>)
+          if (c0 + cstep < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cstep, tok, nxt);
         float v[16];
         for (int r0 = 0; r0 < a.cluster_split; r0 += 4) {
           float p[4][16];
@@ -784,7 +801,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               for (int j = 0; j < 16; ++j) v[j] = (r0 + q == 0) ? p[q][j] : v[j] + p[q][j];
             }
         }
-        epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, v, in);
+        epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
+        if constexpr (kEpiAhead<EPI>) in = nxt;
+        else if (c0 + cstep < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cstep, tok, in);
       }
     }
     cluster_sync();  // keep every piece readable until the sums are done

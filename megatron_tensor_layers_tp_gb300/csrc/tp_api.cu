@@ -164,7 +164,7 @@ GemmPlan plan_gemm(int M) {
   int cols = 32;
   while (cols < 2 * p.BN) cols *= 2;
   p.tmem_cols = cols;
-  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 2 * kSwapMaxTokens * 4;
+  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 4 * kSwapMaxTokens * 4;
   return p;
 }
 

@@ -494,3 +494,113 @@ def split_cache_copies(kcache: dict, dims: Dims, p: Plan) -> List[dict]:
             heads = slice(c, c + 1)
         out.append({b: arr[heads] for b, arr in kcache.items()})
     return out
+
+
+# ---------------------------------------------------------------------------
+# DP attention ("张量、流水线与数据并行", SGLang 的 DP attention): the t ranks of
+# a TP group split into attn_dp attention groups.  Each group batches its own
+# sequences and keeps their KV, with the attention part tensor-parallel over
+# attn_tp = t / attn_dp ranks; the FFN stays tensor-parallel over all t
+# ranks, so the tokens of every group are gathered before it and each group
+# keeps its own rows after it.
+# Readings: sequences are dealt to the groups in contiguous blocks
+# (group k gets sequences [k*ceil(B/attn_dp), ...)); the gather before the FFN
+# is an all-gather of the groups' hidden rows; the FFN's own reduction is the
+# usual all-reduce over t ranks, after which each group takes its rows back
+# (no further traffic).
+# ---------------------------------------------------------------------------
+def attn_tp_size(t: int, attn_dp: int) -> int:
+    """The attention TP width left inside one DP group."""
+    if attn_dp < 1 or t % attn_dp:
+        raise RuleError("attn_dp must divide t")
+    return t // attn_dp
+
+
+def dp_group_of_seq(n_seqs: int, attn_dp: int, b: int) -> int:
+    per = -(-n_seqs // attn_dp)
+    return b // per
+
+
+def kv_bytes_per_rank(n_seqs: int, n_kv_heads: int, head_dim: int, ctx: int, t: int,
+                      attn_dp: int = 1, elem_bytes: int = 2) -> int:
+    """K and V bytes one rank keeps for one layer: its attention group's
+    sequences (all of them under plain TP), and its KV heads among the
+    group's attn_tp ranks (one replicated head when n_kv < attn_tp)."""
+    atp = attn_tp_size(t, attn_dp)
+    heads = n_kv_heads // atp if n_kv_heads >= atp else 1
+    seqs = -(-n_seqs // attn_dp)
+    return seqs * heads * ctx * head_dim * 2 * elem_bytes
+
+
+def dp_gather_received_per_rank(tokens_per_group: Sequence[int], hidden: int,
+                                elem_bytes: int = 2) -> List[int]:
+    """Hidden-row bytes each group's ranks receive from the other groups when
+    the tokens are gathered for the FFN."""
+    total = sum(tokens_per_group)
+    return [(total - n) * hidden * elem_bytes for n in tokens_per_group]
+
+
+def dp_attention_layer_forward(h: Array, W: LayerWeights, kcopies: List[dict],
+                               vcopies: List[dict], batch: Batch, dims: Dims, t: int,
+                               attn_dp: int, rb: Callable = round_bf16) -> Array:
+    """One layer with DP attention.  kcopies / vcopies: the cache copies of
+    the attention plan (attn_tp ranks), indexed [copy][sequence]; a group's
+    ranks touch only its own sequences."""
+    atp = attn_tp_size(t, attn_dp)
+    pa = plan(dims.n_heads, dims.n_kv_heads, dims.intermediate, dims.vocab, atp)
+    pf = plan(dims.n_heads, dims.n_kv_heads, dims.intermediate, dims.vocab, t)
+    n_seqs = int(np.max(batch.seq)) + 1 if len(batch.seq) else 0
+    T = h.shape[0]
+    d = dims.head_dim
+    nq = pa.q_heads_per_rank
+    group = dims.n_heads // dims.n_kv_heads
+    qkv_sh = shard_qkv(W, dims, pa)
+    qkv_b = shard_qkv_bias(W, dims, pa)
+    Wo_sh = shard_rows_by_input(W.wo, atp)
+    h_after = np.empty_like(h)
+    for k in range(attn_dp):
+        rows = np.array([i for i in range(T) if dp_group_of_seq(n_seqs, attn_dp, int(batch.seq[i])) == k],
+                        dtype=np.int64)
+        if len(rows) == 0:
+            continue
+        hk = h[rows]
+        u = rb(rmsnorm(hk, W.attn_norm, dims.rms_eps))
+        parts = []
+        for r in range(atp):                                  # the group's attention ranks
+            y = linear(u, qkv_sh[r], qkv_b[r])
+            kvh = kv_heads_of_rank(pa, dims.n_kv_heads, r)
+            nkv = len(kvh)
+            pos = batch.pos[rows]
+            q = rb(rope(y[:, : nq * d].reshape(len(rows), nq, d), pos, dims.rope_theta))
+            kk = rb(rope(y[:, nq * d:(nq + nkv) * d].reshape(len(rows), nkv, d), pos, dims.rope_theta))
+            v = rb(y[:, (nq + nkv) * d:].reshape(len(rows), nkv, d))
+            c = kv_copy_of_rank(pa, r)
+            for i, row in enumerate(rows):
+                b, p = int(batch.seq[row]), int(batch.pos[row])
+                kcopies[c][b][:, p, :] = kk[i]
+                vcopies[c][b][:, p, :] = v[i]
+            parts.append((q, kvh, c))
+        partials = []
+        for r, (q, kvh, c) in enumerate(parts):
+            o = np.empty((len(rows), nq, d))
+            for i, row in enumerate(rows):
+                b, p = int(batch.seq[row]), int(batch.pos[row])
+                for jl, j in enumerate(q_heads_of_rank(pa, r)):
+                    gl = kvh.index(j // group)
+                    o[i, jl] = attend(q[i, jl], kcopies[c][b][gl, : p + 1], vcopies[c][b][gl, : p + 1])
+            partials.append(linear(rb(o.reshape(len(rows), nq * d)), Wo_sh[r]))
+        red = all_reduce_sum(partials)                          # inside the attention group
+        h_after[rows] = rb(hk + (red if W.bo is None else red + W.bo))
+    # gather every group's rows, FFN over all t ranks, each group keeps its rows
+    u2 = rb(rmsnorm(h_after, W.mlp_norm, dims.rms_eps))
+    gu_sh = shard_gate_up(W, pf)
+    gu_b = shard_gate_up_bias(W, pf)
+    Wd_sh = shard_rows_by_input(W.wd, t)
+    n = pf.inter_per_rank
+    partials = []
+    for r in range(t):
+        y = linear(u2, gu_sh[r], gu_b[r])
+        a = rb(silu(y[:, :n]) * y[:, n:])
+        partials.append(linear(a, Wd_sh[r]))
+    red = all_reduce_sum(partials)
+    return rb(h_after + (red if W.bd is None else red + W.bd))

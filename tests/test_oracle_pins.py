@@ -446,3 +446,58 @@ def test_qk_bias_is_added_before_rope():
     a0 = np.exp(s0) / (np.exp(s0) + np.exp(s1))
     want = np.array([2.0 * a0, 3.0 * (1 - a0), 0.0, 0.0])
     assert np.allclose(out[0], want, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# DP attention ("张量、流水线与数据并行", SGLang 的 DP attention)
+# ---------------------------------------------------------------------------
+def test_attn_tp_width_rule():
+    assert O.attn_tp_size(8, 1) == 8 and O.attn_tp_size(8, 2) == 4 and O.attn_tp_size(8, 8) == 1
+    with pytest.raises(O.RuleError):
+        O.attn_tp_size(8, 3)
+
+
+def test_dp_attention_removes_kv_duplication_for_few_kv_heads():
+    # one KV "head" (the latent head of an MLA-style model): plain TP keeps a
+    # full copy of every sequence's KV on each rank, DP attention splits the
+    # sequences instead
+    B, d, L, t = 64, 512, 1024, 8
+    full = B * 1 * L * d * 2 * 2
+    assert O.kv_bytes_per_rank(B, 1, d, L, t) == full
+    assert O.kv_bytes_per_rank(B, 1, d, L, t, attn_dp=8) == full // 8
+    # 8 KV heads at TP <= 8: nothing is duplicated, so DP attention buys nothing
+    per_rank_tp = O.kv_bytes_per_rank(B, 8, 128, L, 8)
+    assert per_rank_tp * 8 == B * 8 * L * 128 * 2 * 2
+    assert O.kv_bytes_per_rank(B, 8, 128, L, 8, attn_dp=2) == per_rank_tp
+
+
+def test_dp_gather_counts():
+    assert O.dp_gather_received_per_rank([16, 16], 4096) == [16 * 4096 * 2] * 2
+    assert O.dp_gather_received_per_rank([3, 5, 0], 64) == [5 * 128, 3 * 128, 8 * 128]
+
+
+@pytest.mark.parametrize("n_heads,n_kv,t,attn_dp", [(4, 2, 4, 2), (4, 1, 4, 4), (8, 2, 8, 2),
+                                                     (8, 8, 8, 4), (4, 4, 2, 2)])
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("bias", [False, True])
+def test_dp_attention_layer_equals_unsharded(n_heads, n_kv, t, attn_dp, mode, bias):
+    dims, W = _tiny(n_heads, n_kv)
+    if bias:
+        W = _with_biases(dims, W)
+    batch = O.Batch.decode(5, 7) if mode == "decode" else O.Batch.prefill(3, 5)
+    n_seqs = 5 if mode == "decode" else 3
+    L = 7 if mode == "decode" else 5
+    T = len(batch.seq)
+    h = synth.normal_f64(9, 19, (T, dims.hidden), 1.0)
+    kc, vc = _caches(n_seqs, n_kv, L, dims.head_dim)
+    pa = O.plan(n_heads, n_kv, dims.intermediate, dims.vocab, O.attn_tp_size(t, attn_dp))
+    for rb, tol in ((O.no_round, 1e-12), (O.round_bf16, 1e-2)):
+        k1, v1 = _copy(kc), _copy(vc)
+        ref = O.layer_forward(h, W, k1, v1, batch, dims, rb=rb)
+        k2, v2 = _copy(kc), _copy(vc)
+        got = O.dp_attention_layer_forward(h, W, O.split_cache_copies(k2, dims, pa),
+                                           O.split_cache_copies(v2, dims, pa), batch, dims, t,
+                                           attn_dp, rb=rb)
+        assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= tol, (rb, attn_dp)
+        for b in k1:
+            assert np.allclose(k1[b], k2[b], rtol=tol, atol=tol)
