@@ -66,8 +66,19 @@ typedef enum {
  * padded to a multiple of t with zero rows and split evenly.  The
  * intermediate size splits evenly (intermediate % t == 0).
  *
+ * DP attention (P3 SGLang 的 DP attention): attn_dp > 1 splits the t ranks
+ * into attn_dp attention groups of attn_tp = t / attn_dp ranks.  Each group
+ * batches its own sequences (contiguous blocks of the batch) and keeps their
+ * KV; the attention block (qkv_proj, attention, o_proj and its reduction) is
+ * tensor-parallel over the group's attn_tp ranks, while the MLP stays
+ * tensor-parallel over all t ranks, after the groups' hidden rows are
+ * gathered.  The head and KV rules above then apply with attn_tp in place of
+ * t, and the per-rank head fields below describe the attention ranks.
+ * attn_dp = 0 is read as 1 (plain tensor parallelism); t % attn_dp != 0 is
+ * TP_ERR_DIVISIBILITY.
+ *
  * Kernel envelope (TP_ERR_UNSUPPORTED otherwise): head_dim in {64, 128};
- * hidden, n_heads*head_dim/t and intermediate/t multiples of 64;
+ * hidden, n_heads*head_dim/attn_tp and intermediate/t multiples of 64;
  * 1 <= t <= 8; max_positions >= 1. */
 typedef struct {
   int32_t hidden;
@@ -81,14 +92,16 @@ typedef struct {
   float rms_eps;         /* RMSNorm epsilon */
   float rope_theta;      /* RoPE base */
   int32_t max_positions; /* RoPE table length: every position must be < this */
+  int32_t attn_dp;       /* attention data-parallel groups (0 or 1: none) */
   /* derived, written by tp_config */
   int32_t vocab_padded;
   int32_t vocab_per_rank;
   int32_t q_heads_per_rank;
   int32_t kv_heads_per_rank; /* KV heads in one rank's cache (1 when replicated) */
   int32_t kv_replicas;       /* ranks sharing one KV head (1 when split) */
-  int32_t kv_copies;         /* distinct per-rank caches = min(t, n_kv_heads) */
+  int32_t kv_copies;         /* distinct per-rank caches = min(attn_tp, n_kv_heads) */
   int32_t inter_per_rank;
+  int32_t attn_tp;           /* attention ranks per DP group = t / attn_dp */
 } tp_config_t;
 
 /* Validates the shape and fills the derived fields. */
@@ -359,6 +372,8 @@ typedef struct {
   int64_t kernel_launches;     /* kernels launched by the library */
   int64_t stage_sends;         /* pipeline-stage boundaries crossed (tp_stage_send) */
   int64_t stage_send_bytes;    /* bytes handed across them, all ranks together */
+  int64_t dp_gathers;          /* DP attention: token gathers before the MLP (1 per layer) */
+  int64_t dp_gather_recv_bytes_per_rank; /* (attn_dp-1)/attn_dp * M*H*2 per gather */
 } tp_stats_t;
 
 tp_status tp_get_stats(const tp_model* m, tp_stats_t* out);

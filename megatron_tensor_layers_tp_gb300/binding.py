@@ -26,10 +26,11 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 class tp_config_t(Structure):
     _fields_ = [(n, c_int32) for n in ("hidden", "n_heads", "n_kv_heads", "head_dim", "intermediate",
                                        "vocab", "n_layers", "t")] + \
-               [("rms_eps", c_float), ("rope_theta", c_float), ("max_positions", c_int32)] + \
+               [("rms_eps", c_float), ("rope_theta", c_float), ("max_positions", c_int32),
+                ("attn_dp", c_int32)] + \
                [(n, c_int32) for n in ("vocab_padded", "vocab_per_rank", "q_heads_per_rank",
                                        "kv_heads_per_rank", "kv_replicas", "kv_copies",
-                                       "inter_per_rank")]
+                                       "inter_per_rank", "attn_tp")]
 
 
 class tp_layer_weights_t(Structure):
@@ -53,7 +54,8 @@ class tp_batch_t(Structure):
 class tp_stats_t(Structure):
     _fields_ = [(n, c_int64) for n in ("allreduces", "allreduce_payload_bytes", "allgathers",
                                        "allgather_recv_bytes_per_rank", "kernel_launches",
-                                       "stage_sends", "stage_send_bytes")]
+                                       "stage_sends", "stage_send_bytes", "dp_gathers",
+                                       "dp_gather_recv_bytes_per_rank")]
 
 
 class tp_kernel_time_t(Structure):

@@ -18,8 +18,9 @@ using namespace tpk;
 
 struct ShardedLinear {
   uint16_t* data = nullptr;  // [t][rows][cols]
-  uint16_t* bias = nullptr;  // optional: [t][rows] (column-parallel) or [rows] (row-parallel)
+  uint16_t* bias = nullptr;  // optional: [ranks][rows] (column-parallel) or [rows] (row-parallel)
   int rows = 0, cols = 0;    // per rank
+  int ranks = 0;             // t, or attn_tp for the attention block
   CUtensorMap tm_a;          // box (64, 128, 1): weight on the MMA M side (decode)
   CUtensorMap tm_b;          // box (64, 256, 1): weight on the MMA N side (prefill)
 };
@@ -312,7 +313,7 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
   a.BN = p.BN;
   a.stages = p.stages;
   a.tmem_cols = p.tmem_cols;
-  a.n_groups = c.t;
+  a.n_groups = W.ranks;
   a.k_slices = 1;
   a.k_iters_slice = cdiv(K, 64);
   set_schedule(a, p, m->num_sms, epi);
@@ -333,7 +334,7 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
                   uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st) {
   if (M == 0) return TP_OK;
   const tp_config_t& c = m->cfg;
-  const int Kr = W.cols, H = W.rows, t = c.t;
+  const int Kr = W.cols, H = W.rows, t = W.ranks;
   GemmPlan p = plan_gemm(M);
   GemmArgs a;
   memset(&a, 0, sizeof(a));
@@ -407,14 +408,15 @@ bool valid_layer(const tp_model* m, int layer) {
 
 // Builds one sharded weight: t ranks of [rows][cols]; rank r's rows come from
 // the calls the caller makes through `fill` (copy_rows launches).
-tp_status alloc_linear(tp_model* m, ShardedLinear* L, int rows, int cols) {
+tp_status alloc_linear(tp_model* m, ShardedLinear* L, int rows, int cols, int ranks) {
   L->rows = rows;
   L->cols = cols;
-  tp_status s = dev_alloc(m, &L->data, (size_t)m->cfg.t * rows * cols * 2);
+  L->ranks = ranks;
+  tp_status s = dev_alloc(m, &L->data, (size_t)ranks * rows * cols * 2);
   if (s != TP_OK) return s;
   const uint64_t rs = (uint64_t)cols * 2, ss = (uint64_t)rows * cols * 2;
-  if (!make_tmap(&L->tm_a, L->data, cols, rows, m->cfg.t, rs, ss, 128)) return TP_ERR_CUDA;
-  if (!make_tmap(&L->tm_b, L->data, cols, rows, m->cfg.t, rs, ss, kPrefillBN)) return TP_ERR_CUDA;
+  if (!make_tmap(&L->tm_a, L->data, cols, rows, ranks, rs, ss, 128)) return TP_ERR_CUDA;
+  if (!make_tmap(&L->tm_b, L->data, cols, rows, ranks, rs, ss, kPrefillBN)) return TP_ERR_CUDA;
   return TP_OK;
 }
 
@@ -501,26 +503,31 @@ tp_status tp_config(tp_config_t* c) {
       !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
     return TP_ERR_ARG;
   const int t = c->t;
+  if (c->attn_dp < 0) return TP_ERR_ARG;
+  if (c->attn_dp == 0) c->attn_dp = 1;
+  if (t % c->attn_dp) return TP_ERR_DIVISIBILITY;
+  const int at = t / c->attn_dp;  // attention ranks per DP group
   if (c->n_heads % c->n_kv_heads) return TP_ERR_DIVISIBILITY;
-  if (c->n_heads % t) return TP_ERR_DIVISIBILITY;
+  if (c->n_heads % at) return TP_ERR_DIVISIBILITY;
   if (c->intermediate % t) return TP_ERR_DIVISIBILITY;
   int kv_r, reps;
-  if (c->n_kv_heads >= t) {
-    if (c->n_kv_heads % t) return TP_ERR_KV_REPLICA;
-    kv_r = c->n_kv_heads / t;
+  if (c->n_kv_heads >= at) {
+    if (c->n_kv_heads % at) return TP_ERR_KV_REPLICA;
+    kv_r = c->n_kv_heads / at;
     reps = 1;
   } else {
-    if (t % c->n_kv_heads) return TP_ERR_KV_REPLICA;
+    if (at % c->n_kv_heads) return TP_ERR_KV_REPLICA;
     kv_r = 1;
-    reps = t / c->n_kv_heads;
+    reps = at / c->n_kv_heads;
   }
   const int vp = (c->vocab + t - 1) / t * t;
   c->vocab_padded = vp;
   c->vocab_per_rank = vp / t;
-  c->q_heads_per_rank = c->n_heads / t;
+  c->attn_tp = at;
+  c->q_heads_per_rank = c->n_heads / at;
   c->kv_heads_per_rank = kv_r;
   c->kv_replicas = reps;
-  c->kv_copies = std::min(t, c->n_kv_heads);
+  c->kv_copies = std::min(at, c->n_kv_heads);
   c->inter_per_rank = c->intermediate / t;
   // kernel envelope
   if (t > 8) return TP_ERR_UNSUPPORTED;
@@ -603,8 +610,10 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
   if (cudaGetDevice(&m->device) != cudaSuccess) return fail(TP_ERR_CUDA);
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return fail(TP_ERR_CUDA);
-  const int t = cfg.t, H = cfg.hidden, d = cfg.head_dim, nq = cfg.q_heads_per_rank;
-  const int kvr = cfg.kv_heads_per_rank, Ipr = cfg.inter_per_rank;
+  // the attention block is sharded over the attn_tp ranks of a DP group, the
+  // MLP over all t ranks
+  const int t = cfg.t, at = cfg.attn_tp, H = cfg.hidden, d = cfg.head_dim;
+  const int nq = cfg.q_heads_per_rank, kvr = cfg.kv_heads_per_rank, Ipr = cfg.inter_per_rank;
   MapUploader up;
   if ((s = dev_alloc(m, &m->status, 256)) != TP_OK) return fail(s);
   if (cudaMemsetAsync(m->status, 0, 256, st) != cudaSuccess) return fail(TP_ERR_CUDA);
@@ -624,11 +633,11 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
     const tp_layer_weights_t& Wl = w->layers[l];
     LayerShards& Ls = m->layers[l];
     const int nqkv = (nq + 2 * kvr) * d;
-    if ((s = alloc_linear(m, &Ls.qkv, nqkv, H)) != TP_OK) return fail(s);
-    if ((s = alloc_linear(m, &Ls.gate_up, 2 * Ipr, H)) != TP_OK) return fail(s);
-    if ((s = alloc_linear(m, &Ls.o, H, nq * d)) != TP_OK) return fail(s);
-    if ((s = alloc_linear(m, &Ls.down, H, Ipr)) != TP_OK) return fail(s);
-    for (int r = 0; r < t; ++r) {
+    if ((s = alloc_linear(m, &Ls.qkv, nqkv, H, at)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.gate_up, 2 * Ipr, H, t)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.o, H, nq * d, at)) != TP_OK) return fail(s);
+    if ((s = alloc_linear(m, &Ls.down, H, Ipr, t)) != TP_OK) return fail(s);
+    for (int r = 0; r < at; ++r) {
       // qkv: [its Q heads | its KV heads] with RoPE pairs adjacent; V in natural order
       std::vector<int32_t> mq(nq * d), mk(kvr * d), mv(kvr * d);
       for (int hl = 0; hl < nq; ++hl)
@@ -648,18 +657,9 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
           launch_copy_rows(base + (size_t)(nq + kvr) * d * H, H, Wl.wv, H, dv, kvr * d, H, st) !=
               cudaSuccess)
         return fail(TP_ERR_CUDA);
-      // gate_up: row 2j = gate row r*Ipr + j, row 2j+1 = up row r*Ipr + j
-      std::vector<int32_t> mg(Ipr);
-      for (int j = 0; j < Ipr; ++j) mg[j] = r * Ipr + j;
-      int32_t* dg;
-      if ((s = up.upload(mg, &dg, st)) != TP_OK) return fail(s);
-      uint16_t* gbase = Ls.gate_up.data + (size_t)r * 2 * Ipr * H;
-      if (launch_copy_rows(gbase, 2 * H, Wl.wg, H, dg, Ipr, H, st) != cudaSuccess ||
-          launch_copy_rows(gbase + H, 2 * H, Wl.wu, H, dg, Ipr, H, st) != cudaSuccess)
-        return fail(TP_ERR_CUDA);
       // biases follow their rows (one element per row; a missing part is zero)
       if (Wl.bq || Wl.bk || Wl.bv) {
-        if (!Ls.qkv.bias && (s = dev_alloc(m, &Ls.qkv.bias, (size_t)t * nqkv * 2)) != TP_OK)
+        if (!Ls.qkv.bias && (s = dev_alloc(m, &Ls.qkv.bias, (size_t)at * nqkv * 2)) != TP_OK)
           return fail(s);
         int32_t *nq_, *nk_;
         std::vector<int32_t> zq(nq * d, -1), zk(kvr * d, -1);
@@ -673,6 +673,17 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
                 cudaSuccess)
           return fail(TP_ERR_CUDA);
       }
+    }
+    for (int r = 0; r < t; ++r) {
+      // gate_up: row 2j = gate row r*Ipr + j, row 2j+1 = up row r*Ipr + j
+      std::vector<int32_t> mg(Ipr);
+      for (int j = 0; j < Ipr; ++j) mg[j] = r * Ipr + j;
+      int32_t* dg;
+      if ((s = up.upload(mg, &dg, st)) != TP_OK) return fail(s);
+      uint16_t* gbase = Ls.gate_up.data + (size_t)r * 2 * Ipr * H;
+      if (launch_copy_rows(gbase, 2 * H, Wl.wg, H, dg, Ipr, H, st) != cudaSuccess ||
+          launch_copy_rows(gbase + H, 2 * H, Wl.wu, H, dg, Ipr, H, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
       if (Wl.bg || Wl.bu) {
         if (!Ls.gate_up.bias && (s = dev_alloc(m, &Ls.gate_up.bias, (size_t)t * 2 * Ipr * 2)) != TP_OK)
           return fail(s);
@@ -697,13 +708,14 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
     for (int i = 0; i < H; ++i) ident[i] = i;
     int32_t* di;
     if ((s = up.upload(ident, &di, st)) != TP_OK) return fail(s);
-    for (int r = 0; r < t; ++r) {
+    for (int r = 0; r < at; ++r)
       if (launch_copy_rows(Ls.o.data + (size_t)r * H * nq * d, nq * d, Wl.wo + (size_t)r * nq * d,
-                           (int64_t)cfg.n_heads * d, di, H, nq * d, st) != cudaSuccess ||
-          launch_copy_rows(Ls.down.data + (size_t)r * H * Ipr, Ipr, Wl.wd + (size_t)r * Ipr,
+                           (int64_t)cfg.n_heads * d, di, H, nq * d, st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+    for (int r = 0; r < t; ++r)
+      if (launch_copy_rows(Ls.down.data + (size_t)r * H * Ipr, Ipr, Wl.wd + (size_t)r * Ipr,
                            cfg.intermediate, di, H, Ipr, st) != cudaSuccess)
         return fail(TP_ERR_CUDA);
-    }
     if ((s = dev_alloc(m, &Ls.attn_norm, (size_t)H * 2)) != TP_OK ||
         (s = dev_alloc(m, &Ls.mlp_norm, (size_t)H * 2)) != TP_OK)
       return fail(s);
@@ -725,7 +737,7 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
         return fail(TP_ERR_CUDA);
     }
     if (w->lm_head) {
-      if ((s = alloc_linear(m, &m->lm, cfg.vocab_per_rank, H)) != TP_OK) return fail(s);
+      if ((s = alloc_linear(m, &m->lm, cfg.vocab_per_rank, H, t)) != TP_OK) return fail(s);
       if (launch_copy_rows(m->lm.data, H, w->lm_head, H, dmv, cfg.vocab_padded, H, st) != cudaSuccess)
         return fail(TP_ERR_CUDA);
     }
@@ -926,6 +938,12 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   // o_proj (row-parallel) + reduction ① + residual
   if ((s = run_row(m, "gemm_o", Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st)) != TP_OK)
     return s;
+  // DP attention: every group's hidden rows are gathered for the MLP (one
+  // buffer here; counted as each rank receiving the other groups' rows)
+  if (c.attn_dp > 1) {
+    m->stats.dp_gathers++;
+    m->stats.dp_gather_recv_bytes_per_rank += (int64_t)(c.attn_dp - 1) * M * H * 2 / c.attn_dp;
+  }
   // u = RMSNorm(h); gate_up (column-parallel) + SiLU(gate) * up
   TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
     return launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st);
@@ -1058,6 +1076,9 @@ tp_status capture_graph(const tp_model* m, void* stream, tp_graph** out, F&& bod
   g->delta.kernel_launches = after.kernel_launches - before.kernel_launches;
   g->delta.stage_sends = after.stage_sends - before.stage_sends;
   g->delta.stage_send_bytes = after.stage_send_bytes - before.stage_send_bytes;
+  g->delta.dp_gathers = after.dp_gathers - before.dp_gathers;
+  g->delta.dp_gather_recv_bytes_per_rank =
+      after.dp_gather_recv_bytes_per_rank - before.dp_gather_recv_bytes_per_rank;
   *out = g;
   return TP_OK;
 }
@@ -1093,6 +1114,8 @@ tp_status tp_graph_launch(tp_graph* g, void* stream) {
   s.kernel_launches += g->delta.kernel_launches;
   s.stage_sends += g->delta.stage_sends;
   s.stage_send_bytes += g->delta.stage_send_bytes;
+  s.dp_gathers += g->delta.dp_gathers;
+  s.dp_gather_recv_bytes_per_rank += g->delta.dp_gather_recv_bytes_per_rank;
   return TP_OK;
 }
 

@@ -26,11 +26,13 @@ def _stream(stream) -> int:
 
 
 def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, n_layers, t,
-                rms_eps=1e-5, rope_theta=10000.0, max_positions=8192) -> B.tp_config_t:
+                rms_eps=1e-5, rope_theta=10000.0, max_positions=8192,
+                attn_dp=1) -> B.tp_config_t:
     c = B.tp_config_t()
     c.hidden, c.n_heads, c.n_kv_heads, c.head_dim = hidden, n_heads, n_kv_heads, head_dim
     c.intermediate, c.vocab, c.n_layers, c.t = intermediate, vocab, n_layers, t
     c.rms_eps, c.rope_theta, c.max_positions = rms_eps, rope_theta, max_positions
+    c.attn_dp = attn_dp
     return c
 
 
@@ -141,7 +143,8 @@ class TPModel:
     def column_linear(self, layer: int, which: int, x: torch.Tensor, stream=None) -> torch.Tensor:
         M = x.shape[0]
         n = self.qkv_rows() if which == B.TP_QKV else 2 * self.cfg.inter_per_rank
-        y = torch.empty((self.cfg.t, M, n), dtype=torch.bfloat16, device="cuda")
+        ranks = self.cfg.attn_tp if which == B.TP_QKV else self.cfg.t
+        y = torch.empty((ranks, M, n), dtype=torch.bfloat16, device="cuda")
         self.ensure_workspace(M, stream)
         B.check(B.tp_column_linear(self.handle, layer, which, x.data_ptr(), M, y.data_ptr(), M * n,
                                    *self.ws_args, _stream(stream)), "tp_column_linear")
@@ -152,7 +155,7 @@ class TPModel:
                           stream=None) -> torch.Tensor:
         """x: [M, t*K_r] (rank r's shard in columns [r K_r, (r+1) K_r))."""
         M = x.shape[0]
-        t = self.cfg.t
+        t = self.cfg.attn_tp if which == B.TP_O else self.cfg.t
         kr = x.shape[1] // t
         y = out if out is not None else torch.empty((M, self.cfg.hidden), dtype=torch.bfloat16,
                                                     device="cuda")

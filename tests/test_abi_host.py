@@ -82,3 +82,26 @@ def test_calls_without_a_model_are_rejected_on_the_host():
     assert B.lib().tp_get_stats(None, None) == ST["TP_ERR_ARG"]
     for code, name in B.STATUS_NAMES.items():
         assert B.strerror(code) and B.strerror(code) != "unknown status", name
+
+
+def test_dp_attention_config_rules():
+    # attention ranks per group = t / attn_dp; head and KV rules against them
+    c = make_config(4096, 32, 8, 128, 14336, 1000, 1, 8, attn_dp=2)
+    assert B.tp_config(c) == B.TP_OK
+    assert (c.attn_tp, c.q_heads_per_rank, c.kv_heads_per_rank, c.kv_replicas, c.kv_copies,
+            c.inter_per_rank) == (4, 8, 2, 1, 4, 1792)
+    c = make_config(2048, 16, 1, 128, 14336, 1000, 1, 8, attn_dp=8)
+    assert B.tp_config(c) == B.TP_OK
+    assert (c.attn_tp, c.q_heads_per_rank, c.kv_heads_per_rank, c.kv_replicas, c.kv_copies) == \
+        (1, 16, 1, 1, 1)
+    c = make_config(4096, 32, 2, 128, 14336, 1000, 1, 8, attn_dp=2)
+    assert B.tp_config(c) == B.TP_OK
+    assert (c.attn_tp, c.kv_heads_per_rank, c.kv_replicas, c.kv_copies) == (4, 1, 2, 2)
+    c = make_config(4096, 32, 8, 128, 14336, 1000, 1, 8, attn_dp=3)
+    assert B.tp_config(c) == B.STATUS["TP_ERR_DIVISIBILITY"]
+    c = make_config(4096, 32, 8, 128, 14336, 1000, 1, 8, attn_dp=0)
+    assert B.tp_config(c) == B.TP_OK and c.attn_dp == 1 and c.attn_tp == 8
+    # the same shapes from the oracle's plan
+    import oracle as O
+    p = O.plan(32, 8, 14336, 1000, O.attn_tp_size(8, 2))
+    assert (p.q_heads_per_rank, p.kv_heads_per_rank, p.kv_replicas, p.kv_copies) == (8, 2, 1, 4)
