@@ -95,6 +95,24 @@ def measured_traffic(kernel):
     return k["dram_bytes_per_launch"] if k else None
 
 
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest of every rank's x (one all-reduce; the replicas share no
+    data, this only joins their clocks)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    tm = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    return float(tm.item())
+
+
+def whole_job_rate(units_per_rank: int, steps: int, ms_max: float, world: int) -> float:
+    """Units per second of the whole job: every replica processes the same
+    units per step, and the job takes as long as its slowest replica."""
+    return world * units_per_rank * steps / (ms_max / 1e3)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -284,14 +302,11 @@ def run_ours(args, rank, world):
     prof_steps = min(args.steps, 2000)
     ms_prof, prof, _ = timed_steps(model, batch, h, prof_steps, 0, args.rotate, args.fused,
                                    stream, profile=True)
-    if world > 1:
-        tm = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(ms, world)
     assert model.check_device(stream) == 0, "device status word set"
     ms_step = ms / args.steps
     tokens = w.tokens
-    value = world * tokens * args.steps / (ms / 1e3)
+    value = whole_job_rate(tokens, args.steps, ms, world)
 
     kb, step_bytes = layer_bytes(w, args.t)
     kernels = {}
@@ -386,12 +401,8 @@ def run_ours(args, rank, world):
             hout.copy_(h, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        tm = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms_e2e = float(tm.item())
-    e2e = {"value": round(world * tokens * e2e_steps / (ms_e2e / 1e3), 1), "unit": UNIT,
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": round(whole_job_rate(tokens, e2e_steps, ms_e2e, world), 1), "unit": UNIT,
            "h2d_bytes_per_step": w.tokens * w.hidden * 2, "d2h_bytes_per_step": w.tokens * w.hidden * 2,
            "steps": e2e_steps}
 
