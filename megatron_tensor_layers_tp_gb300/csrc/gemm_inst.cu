@@ -28,8 +28,10 @@ cudaError_t TPK_CAT(launch_gemm_epi, TPK_EPI)(bool swap, const GemmArgs& a, size
   if (e != cudaSuccess) return e;
   const int cx = a.cluster_split > 1 ? a.cluster_split : 1;
   if (swap)
-    return launch_kc(gemm_kernel<true, TPK_EPI>, dim3(a.grid), dim3(kThreads), smem, st, cx, a);
-  return launch_kc(gemm_kernel<false, TPK_EPI>, dim3(a.grid), dim3(kThreads), smem, st, cx, a);
+    return launch_kc(gemm_kernel<true, TPK_EPI>, dim3(a.grid), dim3(kThreadsOf<true>), smem, st,
+                     cx, a);
+  return launch_kc(gemm_kernel<false, TPK_EPI>, dim3(a.grid), dim3(kThreadsOf<false>), smem, st,
+                   cx, a);
 }
 
 // How many clusters of cluster_x CTAs (smem bytes each) can be resident at once.
@@ -37,7 +39,7 @@ int TPK_CAT(gemm_max_clusters_epi, TPK_EPI)(bool swap, int cluster_x, size_t sme
   if ((swap ? set_smem_attr<true>() : set_smem_attr<false>()) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster_x * 64);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(swap ? kThreadsOf<true> : kThreadsOf<false>);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -26,7 +26,6 @@
 
 namespace tpk {
 
-constexpr int kThreads = 192;
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
 __device__ __forceinline__ uint64_t make_policy(int kind) {
@@ -81,6 +80,17 @@ struct EpiIn {
 
 // Epilogues that add the GEMM's output bias (the unfused row-parallel
 // partials leave it to the rank reduction; the LM head has none).
+// Columns one epilogue thread finishes at a time: 8 tokens in the decode
+// orientation (two warps share each TMEM lane quadrant, each taking alternate
+// 8-column units), 16 features in the prefill orientation.
+template <bool SWAP>
+constexpr int kUnit = SWAP ? 8 : 16;
+// epilogue warps: 8 in the decode orientation, 4 in the prefill orientation
+template <bool SWAP>
+constexpr int kEpiWarps = SWAP ? 8 : 4;
+template <bool SWAP>
+constexpr int kThreadsOf = (2 + kEpiWarps<SWAP>) * 32;
+
 template <int EPI>
 constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || EPI == EPI_RESID;
 // Multi-chunk epilogues fetch the next chunk's inputs before storing the
@@ -109,7 +119,7 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
   }
   if constexpr (SWAP && EPI == EPI_RESID) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < kUnit<SWAP>; ++j) {
       const int m = brow0 + j;
       in.r[j] = (e.residual && fval && m < e.M) ? bf16_to_f(e.residual[(int64_t)m * e.ld_res + f])
                                                 : 0.f;
@@ -119,12 +129,12 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
     if (fval) qkv_classify(e, f, kind, head, w);
     const int half = e.head_dim / 2, jp = w >> 1;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < kUnit<SWAP>; ++j) {
       const int m = brow0 + j;
       in.pos[j] = (fval && m < e.M) ? tok[m] : -1;
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < kUnit<SWAP>; ++j) {
       const bool ok = in.pos[j] >= 0 && in.pos[j] < e.l_max;
       in.cs[j] = (ok && kind != 2) ? e.rope[(int64_t)in.pos[j] * half + jp] : make_float2(1.f, 0.f);
     }
@@ -161,7 +171,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
   if constexpr (kEpiBias<EPI>) {
     if (e.bias) {  // before RoPE / SiLU pairing and the residual
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] += SWAP ? in.b[0] : in.b[j];
+      for (int j = 0; j < kUnit<SWAP>; ++j) v[j] += SWAP ? in.b[0] : in.b[j];
     }
   }
   if constexpr (SWAP) {
@@ -173,14 +183,14 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       // loads are not serialised behind stores to the same buffer.
       uint16_t* out = static_cast<uint16_t*>(e.out);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const int m = brow0 + j;
         if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + in.r[j]);
       }
     } else if constexpr (EPI == EPI_PARTIAL) {
       float* out = static_cast<float*>(e.out) + (int64_t)g * e.out_group_stride;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const int m = brow0 + j;
         if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = v[j];
       }
@@ -188,7 +198,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)g * e.out_group_stride;
       const int col = fval ? plain_col(e, f) : 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const int m = brow0 + j;
         if (fval && m < e.M) out[(int64_t)m * e.ld_out + col] = f_to_bf16(v[j]);
       }
@@ -197,7 +207,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       const int64_t col = (int64_t)g * e.vocab_per_rank + f;
       const bool ok = fval && f < e.vocab_per_rank && col < e.vocab;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const int m = brow0 + j;
         if (ok && m < e.M) out[(int64_t)m * e.ld_out + col] = f_to_bf16(v[j]);
       }
@@ -205,7 +215,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       uint16_t* out = static_cast<uint16_t*>(e.out);
       const int64_t col = (int64_t)g * e.inter_per_rank + (f >> 1);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
         const int m = brow0 + j;
         if (fval && !(f & 1) && m < e.M) {
@@ -228,7 +238,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       uint16_t* cache_row = (kind == 1 ? e.k_cache : e.v_cache) + copy * e.kv_copy_stride +
                             (int64_t)head * e.l_max * d + feat;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
         const float partner = __shfl_xor_sync(0xffffffffu, v[j], 1);
         const int m = brow0 + j;
         if (!fval || m >= e.M) continue;
@@ -420,7 +430,7 @@ struct SegIter {
 };
 
 template <bool SWAP, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
+__global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -440,7 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps<SWAP>);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -586,9 +599,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else {
     pdl_wait();
     if constexpr (EPI == EPI_QKV) pdl_launch_dependents();
+    // Epilogue warp w reads TMEM lanes of quadrant w % 4 (its 32 rows); in the
+    // decode orientation two warps share a quadrant and take alternate
+    // U-column units of every 16-column span.
+    constexpr int U = kUnit<SWAP>, NH = kEpiWarps<SWAP> / 4, ET = kEpiWarps<SWAP> * 32;
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
-    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
+    const int et = threadIdx.x - 64;  // 0..ET-1 over the epilogue warps
+    auto tld = [&](uint32_t addr, float (&v)[16]) {
+      if constexpr (SWAP) tmem_ld8(addr, v);
+      else tmem_ld16(addr, v);
+    };
     if constexpr (SWAP && EPI == EPI_QKV) {
       // every tile of the decode orientation covers tokens 0..M-1
       if (et < kSwapMaxTokens) {
@@ -600,13 +622,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         reinterpret_cast<int64_t*>(tok + 2 * kSwapMaxTokens)[et] =
             ((int64_t)seq * a.e.kv_heads_per_rank * a.e.l_max + pos) * a.e.head_dim;
       }
-      bar_sync(1, 128);
+      bar_sync(1, ET);
     }
-    // chunks of 16 columns this CTA finishes itself: all of them, except in a
-    // cluster split where rank r sums and stores chunks r, r + s, ...
+    // units this thread stores itself: columns c0 = u0, u0 + ustep, ... of a
+    // tile; in a cluster split the (half, rank) workers of the cluster share
+    // the units of the one tile
     const int rank = a.cluster_split > 1 ? static_cast<int>(c % a.cluster_split) : 0;
-    const int chunk0 = a.cluster_split > 1 ? rank * 16 : 0;
-    const int chunk_step = a.cluster_split > 1 ? a.cluster_split * 16 : 16;
+    const int worker = half * (a.cluster_split > 1 ? a.cluster_split : 1) + rank;
+    const int u0 = worker * U;
+    const int ustep = NH * (a.cluster_split > 1 ? a.cluster_split : 1) * U;
+    const int chunk0 = a.cluster_split > 1 ? u0 : half * U;
     {
       SegIter t = make_iter();
       Segment last, x;
@@ -629,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&acc_full[buf], use & 1, a.status);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (bar_sync_or(1, 128, !ok)) break;
+      if (bar_sync_or(1, ET, !ok)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
       const int arow = ia * 128 + row;
@@ -639,12 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // operand stages are free: every load was consumed by the finished
         // MMAs); the pieces are summed after the cluster barrier
         float* red = reinterpret_cast<float*>(smem);
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = half * U; c0 < BN; c0 += NH * U) {
           float v[16];
-          tmem_ld16(taddr + c0, v);
+          tld(taddr + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + row] = v[j];
+          for (int j = 0; j < kUnit<SWAP>; ++j) red[(c0 + j) * 128 + row] = v[j];
         }
         tc_fence_before();
         __syncwarp();
@@ -662,12 +687,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       if (nseg == 1) {
         if constexpr (SWAP) {
-          for (int c0 = 0; c0 < BN; c0 += 16) {
+          for (int c0 = half * U; c0 < BN; c0 += NH * U) {
             float v[16];
             EpiIn in;
-            if (use_pre && c0 == 0) in = pre;
+            if (use_pre && c0 == half * U) in = pre;
             else epi_load<SWAP, EPI>(a, g, arow, brow + c0, tok, in);
-            tmem_ld16(taddr + c0, v);
+            tld(taddr + c0, v);
             tmem_ld_wait();
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
           }
@@ -678,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int c0 = 0; c0 < BN; c0 += 16) {
             if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
             float v[16];
-            tmem_ld16(taddr + c0, v);
+            tld(taddr + c0, v);
             tmem_ld_wait();
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, cur);
             cur = nxt;
@@ -691,23 +716,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // my piece of the tile -> workspace slot 0 (tile where my range starts) or 1
         const int my_slot = (beg / K == ts) ? 0 : 1;
         float* mine = a.partials + ((int64_t)(c * 2 + my_slot) * BN) * 128;
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = half * U; c0 < BN; c0 += NH * U) {
           float v[16];
-          tmem_ld16(taddr + c0, v);
+          tld(taddr + c0, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mine[(c0 + j) * 128 + row] = v[j];
+          for (int j = 0; j < kUnit<SWAP>; ++j) mine[(c0 + j) * 128 + row] = v[j];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         __threadfence();
-        bar_sync(1, 128);
+        bar_sync(1, ET);
         if (threadIdx.x == 64) {
           const int old = atomicAdd(&a.tickets[sg.tile], 1);
           *last_flag = (old == nseg - 1) ? 1 : 0;
         }
-        bar_sync(1, 128);
+        bar_sync(1, ET);
         if (*last_flag) {
           __threadfence();
           // The pieces in K order are those of CTAs c_first, c_first + 1, ...;
@@ -726,38 +751,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const float* src = base + ((int64_t)pq * 2 + (pq == 0 ? slot0 : 0)) * BN * 128 +
                                    c0 * 128;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) tmp[q][j] = __ldcg(src + j * 128);
+                for (int j = 0; j < kUnit<SWAP>; ++j) tmp[q][j] = __ldcg(src + j * 128);
               }
             }
           };
-          load_batch(0, 0);
-          EpiIn in;  // inputs of the current chunk; those of the next are fetched ahead
+          const int cs = NH * U;  // this thread's units: half * U, + cs, ...
+          load_batch(half * U, 0);
+          EpiIn in;  // inputs of the current unit; those of the next are fetched ahead
           if (use_pre) in = pre;
-          else epi_load<SWAP, EPI>(a, g, arow, brow, tok, in);
-          for (int c0 = 0; c0 < BN; c0 += 16) {
+          else epi_load<SWAP, EPI>(a, g, arow, brow + half * U, tok, in);
+          for (int c0 = half * U; c0 < BN; c0 += cs) {
             EpiIn nxt;
             if constexpr (kEpiAhead<EPI>)
-              if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
+              if (c0 + cs < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cs, tok, nxt);
             float v[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int j = 0; j < kUnit<SWAP>; ++j) v[j] = 0.f;
             for (int s0 = 0; s0 < nseg; s0 += 4) {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 if (s0 + q < nseg) {
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) v[j] += tmp[q][j];
+                  for (int j = 0; j < kUnit<SWAP>; ++j) v[j] += tmp[q][j];
                 }
               if (s0 + 4 < nseg) load_batch(c0, s0 + 4);
-              else if (c0 + 16 < BN) load_batch(c0 + 16, 0);
+              else if (c0 + cs < BN) load_batch(c0 + cs, 0);
             }
             epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
             if constexpr (kEpiAhead<EPI>) in = nxt;
-            else if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, in);
+            else if (c0 + cs < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cs, tok, in);
           }
           if (threadIdx.x == 64) a.tickets[sg.tile] = 0;
         }
-        bar_sync(1, 128);
+        bar_sync(1, ET);
       }
       ++seg;
     }
@@ -767,7 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // every thread of the cluster: the pieces are in shared memory
     cluster_sync();
     if (warp >= 2) {
+      constexpr int U = kUnit<SWAP>, NH = kEpiWarps<SWAP> / 4;
       const int rank = static_cast<int>(c % a.cluster_split);
+      const int half = (warp - 2) >> 2;
       const int row = (warp & 3) * 32 + lane;
       const int64_t tile = c / a.cluster_split;
       int g, ia, ib;
@@ -776,11 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t red_s = smem_u32(smem);
       // rank r sums and stores chunks r, r + s, ...; the pieces are added in
       // K order (rank 0 first), up to 4 remote loads in flight together
-      const int cstep = a.cluster_split * 16;
-      EpiIn in;  // inputs of the current chunk; those of the next are fetched ahead
+      // worker (half, rank) sums units c0 = (half * s + rank) * U, + NH * s * U, ...
+      const int cfirst = (half * a.cluster_split + rank) * U;
+      const int cstep = NH * a.cluster_split * U;
+      EpiIn in;  // inputs of the current unit; those of the next are fetched ahead
       if (pre_ok) in = pre;
-      else if (rank * 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + rank * 16, tok, in);
-      for (int c0 = rank * 16; c0 < BN; c0 += cstep) {
+      else if (cfirst < BN) epi_load<SWAP, EPI>(a, g, arow, brow + cfirst, tok, in);
+      for (int c0 = cfirst; c0 < BN; c0 += cstep) {
         EpiIn nxt;
         if constexpr (kEpiAhead<EPI>)
           if (c0 + cstep < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cstep, tok, nxt);
@@ -791,14 +821,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int q = 0; q < 4; ++q)
             if (r0 + q < a.cluster_split) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
+              for (int j = 0; j < kUnit<SWAP>; ++j)
                 p[q][j] = ld_shared_cluster(mapa_shared(red_s + ((c0 + j) * 128 + row) * 4, r0 + q));
             }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             if (r0 + q < a.cluster_split) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = (r0 + q == 0) ? p[q][j] : v[j] + p[q][j];
+              for (int j = 0; j < kUnit<SWAP>; ++j) v[j] = (r0 + q == 0) ? p[q][j] : v[j] + p[q][j];
             }
         }
         epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
