@@ -183,7 +183,7 @@ struct DecSmem {
   // from the one it wants).
   static constexpr int kStages = D == 128 ? 4 : 8;
   static_assert(kStages % kDecGroups == 0, "stages must split evenly between the warp groups");
-  static constexpr int kComb = kDecGroupWarps * 16 * (D + 2);  // floats: O, m, l per warp/row
+  static constexpr int kComb = kDecWarps * 16 * (D + 2);  // floats: O, m, l per warp/row
   static constexpr size_t bytes(int) {
     return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
   }
@@ -330,61 +330,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
       }
-      // combine: the second group's (m, l, O) is folded into the first
-      // group's registers (same fragment layout), then the four merged
-      // states meet in smem
-      float* cw = comb + wq * 16 * (D + 2);
+      // combine: every warp's (m, l, O) meets the others in smem
+      float* cw = comb + warp * 16 * (D + 2);
       const int r0 = lane >> 2;
-      if (grp == 1) {
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          const int col = nt * 8 + (lane & 3) * 2;
-          cw[r0 * (D + 2) + col] = o[nt][0];
-          cw[r0 * (D + 2) + col + 1] = o[nt][1];
-          cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
-          cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
-        }
-        if ((lane & 3) == 0) {
-          cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
-          cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
-        }
+      for (int nt = 0; nt < D / 8; ++nt) {
+        const int col = nt * 8 + (lane & 3) * 2;
+        *reinterpret_cast<float2*>(cw + r0 * (D + 2) + col) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(cw + (r0 + 8) * (D + 2) + col) = make_float2(o[nt][2], o[nt][3]);
       }
-      bar_sync(1, kDecWarps * 32);
-      if (grp == 0) {
-        float sa[2], sb[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float mb = cw[(r0 + 8 * h) * (D + 2) + D];
-          const float lb = cw[(r0 + 8 * h) * (D + 2) + D + 1];
-          const float mn = fmaxf(m[h], mb);
-          sa[h] = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mn);
-          sb[h] = mb == -INFINITY ? 0.f : exp2f(mb - mn);
-          l[h] = l[h] * sa[h] + lb * sb[h];
-          m[h] = mn;
-        }
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          const int col = nt * 8 + (lane & 3) * 2;
-          o[nt][0] = o[nt][0] * sa[0] + cw[r0 * (D + 2) + col] * sb[0];
-          o[nt][1] = o[nt][1] * sa[0] + cw[r0 * (D + 2) + col + 1] * sb[0];
-          o[nt][2] = o[nt][2] * sa[1] + cw[(r0 + 8) * (D + 2) + col] * sb[1];
-          o[nt][3] = o[nt][3] * sa[1] + cw[(r0 + 8) * (D + 2) + col + 1] * sb[1];
-        }
-      }
-      bar_sync(1, kDecWarps * 32);
-      if (grp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          const int col = nt * 8 + (lane & 3) * 2;
-          cw[r0 * (D + 2) + col] = o[nt][0];
-          cw[r0 * (D + 2) + col + 1] = o[nt][1];
-          cw[(r0 + 8) * (D + 2) + col] = o[nt][2];
-          cw[(r0 + 8) * (D + 2) + col + 1] = o[nt][3];
-        }
-        if ((lane & 3) == 0) {
-          cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
-          cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
-        }
+      if ((lane & 3) == 0) {
+        cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
+        cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
       // row = ct / 8, 16 columns each (D = 128) or 8 (D = 64); the second
@@ -395,12 +352,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       const int row = ct >> 3, c0 = (ct & 7) * CPT;
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecGroupWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
+      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
       float ll = 0.f, acc[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecGroupWarps; ++w) {
+      for (int w = 0; w < kDecWarps; ++w) {
         const float* cr = comb + (w * 16 + row) * (D + 2);
         const float mw = cr[D];
         if (mw == -INFINITY) continue;

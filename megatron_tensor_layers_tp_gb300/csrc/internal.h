@@ -155,8 +155,11 @@ size_t attn_decode_smem_bytes(int head_dim);
 cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,
                          const int32_t* ids, int M, int H, uint16_t* h, int* status,
                          cudaStream_t st);
+// w_loaded: w is a model weight written at load time (read before the
+// dependency wait); otherwise it is read after it
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
-                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st);
+                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st,
+                           bool w_loaded);
 cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int t, int M, int H,
                                 const uint16_t* bias, const uint16_t* residual, uint16_t* y,
                                 cudaStream_t st);

@@ -63,28 +63,66 @@ cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, i
 // row i of y normalises row rows[i] of x (the sampled rows before the head).
 // ---------------------------------------------------------------------------
 constexpr int kNormThreads = 256;
+constexpr int kNormVec = 4;  // 16-byte vectors a thread keeps in registers (H <= 8192)
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
     const uint16_t* __restrict__ x, int64_t ldx, const int32_t* __restrict__ rows,
-    const uint16_t* __restrict__ w, int H, float eps, uint16_t* __restrict__ y, int64_t ldy) {
+    const uint16_t* __restrict__ w, int H, float eps, uint16_t* __restrict__ y, int64_t ldy,
+    bool w_loaded) {
   __shared__ float red[kNormThreads / 32];
   pdl_launch_dependents();
-  pdl_wait();
   const int i = blockIdx.x;
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  const int nvec = H / 8;
+  const bool cached = nvec <= kNormVec * kNormThreads;
+  // a model's norm weight is written once, when the model is loaded
+  // (w_loaded): then it is fetched before waiting for the kernel that wrote x
+  uint4 wv[kNormVec], xv[kNormVec];
+  auto load_w = [&]() {
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      const int v = threadIdx.x + k * kNormThreads;
+      if (v < nvec) wv[k] = wr[v];
+    }
+  };
+  if (cached && w_loaded) load_w();
+  pdl_wait();
+  if (cached && !w_loaded) load_w();
   const int src_row = rows ? rows[i] : i;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)src_row * ldx);
-  const uint4* wr = reinterpret_cast<const uint4*>(w);
   uint4* yr = reinterpret_cast<uint4*>(y + (int64_t)i * ldy);
-  const int nvec = H / 8;
-  float ss = 0.f;
-  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
-    const uint4 p = xr[v];
+  auto sumsq = [](const uint4& p, float ss) {
     const uint16_t* e = reinterpret_cast<const uint16_t*>(&p);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float f = bf16_to_f(e[j]);
       ss = fmaf(f, f, ss);
     }
+    return ss;
+  };
+  auto scaled = [](const uint4& p, const uint4& q, float inv) {
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&p);
+    const uint16_t* g = reinterpret_cast<const uint16_t*>(&q);
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      op[j] = pack_bf16x2(bf16_to_f(e[2 * j]) * inv * bf16_to_f(g[2 * j]),
+                          bf16_to_f(e[2 * j + 1]) * inv * bf16_to_f(g[2 * j + 1]));
+    return o;
+  };
+  float ss = 0.f;
+  if (cached) {  // one pass over x: its vectors stay in registers
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k) {
+      const int v = threadIdx.x + k * kNormThreads;
+      if (v < nvec) xv[k] = xr[v];
+    }
+#pragma unroll
+    for (int k = 0; k < kNormVec; ++k)
+      if (threadIdx.x + k * kNormThreads < nvec) ss = sumsq(xv[k], ss);
+  } else {
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) ss = sumsq(xr[v], ss);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -94,25 +132,23 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(
 #pragma unroll
   for (int k = 0; k < kNormThreads / 32; ++k) tot += red[k];
   const float inv = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int v = threadIdx.x; v < nvec; v += kNormThreads) {
-    const uint4 p = xr[v], q = wr[v];
-    const uint16_t* e = reinterpret_cast<const uint16_t*>(&p);
-    const uint16_t* g = reinterpret_cast<const uint16_t*>(&q);
-    uint4 o;
-    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+  if (cached) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      op[j] = pack_bf16x2(bf16_to_f(e[2 * j]) * inv * bf16_to_f(g[2 * j]),
-                          bf16_to_f(e[2 * j + 1]) * inv * bf16_to_f(g[2 * j + 1]));
-    yr[v] = o;
+    for (int k = 0; k < kNormVec; ++k) {
+      const int v = threadIdx.x + k * kNormThreads;
+      if (v < nvec) yr[v] = scaled(xv[k], wv[k], inv);
+    }
+  } else {
+    for (int v = threadIdx.x; v < nvec; v += kNormThreads) yr[v] = scaled(xr[v], wr[v], inv);
   }
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int64_t ldx, const int32_t* rows, const uint16_t* w,
-                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st) {
+                           int M, int H, float eps, uint16_t* y, int64_t ldy, cudaStream_t st,
+                           bool w_loaded) {
   if (M == 0) return cudaSuccess;
   return launch_k(rmsnorm_kernel, dim3(M), dim3(kNormThreads), 0, st, x, ldx, rows, w, H, eps, y,
-                  ldy);
+                  ldy, w_loaded);
 }
 
 // ---------------------------------------------------------------------------

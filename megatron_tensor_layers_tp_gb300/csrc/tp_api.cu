@@ -839,7 +839,7 @@ tp_status tp_rmsnorm(const tp_model* m, const tp_bf16* x, const tp_bf16* w, int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return cuda_status(launch(m, "rmsnorm", st, [&] {
     return launch_rmsnorm(x, m->cfg.hidden, nullptr, w, M, m->cfg.hidden, m->cfg.rms_eps, y,
-                          m->cfg.hidden, st);
+                          m->cfg.hidden, st, false);
   }));
 }
 
@@ -874,7 +874,7 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   tp_status s;
   // u = RMSNorm(h)
   TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
-    return launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st);
+    return launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st, true);
   }));
   // qkv (column-parallel) + RoPE + K/V into the rank caches
   EpiArgs e = base_epi(m, M);
@@ -946,7 +946,7 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   }
   // u = RMSNorm(h); gate_up (column-parallel) + SiLU(gate) * up
   TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
-    return launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st);
+    return launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st, true);
   }));
   EpiArgs e2 = base_epi(m, M);
   e2.out = act;
@@ -993,7 +993,7 @@ static tp_status stage_forward(const tp_model* m, int first, int n, const int32_
   uint16_t* hs = at<uint16_t>(ws, L.hs);
   TP_CHECK_CUDA(launch(m, "rmsnorm_final", st, [&] {
     return launch_rmsnorm(h, m->cfg.hidden, b->sample_rows, m->final_norm, b->n_samples,
-                          m->cfg.hidden, m->cfg.rms_eps, hs, m->cfg.hidden, st);
+                          m->cfg.hidden, m->cfg.rms_eps, hs, m->cfg.hidden, st, true);
   }));
   EpiArgs e = base_epi(m, b->n_samples);
   e.out = logits;
