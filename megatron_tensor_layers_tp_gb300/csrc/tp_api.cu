@@ -185,10 +185,11 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   a.cluster_split = 1;
   if (p.swap) {
     // the largest cluster (8 CTAs at most, portable) whose tiles x s CTAs fill
-    // at least 80% of the SMs in one wave; the occupancy query decides
-    // whether that many clusters are co-resident on this part's GPCs
+    // at least 65% of the SMs in one wave (measured: a cluster split beats
+    // stream-K's fix-up from there on); the occupancy query decides whether
+    // that many clusters are co-resident on this part's GPCs
     for (int s = 8; s >= 2; --s) {
-      if (n_tiles * s > num_sms || n_tiles * s * 5 < (int64_t)num_sms * 4 || K < 2 * s) continue;
+      if (n_tiles * s > num_sms || n_tiles * s * 100 < (int64_t)num_sms * 65 || K < 2 * s) continue;
       if (gemm_max_clusters(true, epi, s, p.smem) < n_tiles) continue;
       a.cluster_split = s;
       a.dp_waves = 0;

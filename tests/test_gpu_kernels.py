@@ -234,10 +234,13 @@ def test_prefill_orientation_schedules_match_oracle(M, inter, t):
 
 @pytest.mark.parametrize("t", [1, 2, 8])
 @pytest.mark.parametrize("M", [1, 16, 64])
-def test_decode_cluster_split_matches_oracle(t, M):
-    # hidden 4096: 32 row-parallel output tiles and 48 qkv tiles, which the
-    # decode schedule splits over clusters of CTAs (K pieces summed on chip)
-    w = _wl(hidden=4096, n_heads=32, n_kv=8, head_dim=128, inter=2048)
+@pytest.mark.parametrize("hidden,n_heads", [(4096, 32), (5120, 40)])
+def test_decode_cluster_split_matches_oracle(t, M, hidden, n_heads):
+    # hidden 4096: 32 row-parallel output tiles (clusters of 4) and 48 qkv
+    # tiles; hidden 5120: 40 row-parallel tiles (clusters of 3) and 56 qkv
+    # tiles (clusters of 2) -- the decode schedule splits them over clusters
+    # of CTAs whose K pieces are summed on chip
+    w = _wl(hidden=hidden, n_heads=n_heads, n_kv=8, head_dim=128, inter=2048)
     m, _, _ = _model(w, t, head=False)
     W = oracle_layer(w, 0)
     x = _x(M, w.hidden, seed=51)
