@@ -182,3 +182,18 @@ def test_two_layer_forward_with_padded_vocab_and_counters():
     assert logits.shape == (w.n_seqs, w.vocab)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
+
+
+@pytest.mark.parametrize("n_seqs", [1, 7, 16])
+def test_decode_layer_4096_wide_ragged_tokens_matches_oracle(n_seqs):
+    # hidden 4096: o_proj and down_proj run as 32 clusters of 4 CTAs, qkv and
+    # gate_up as stream-K, at 1, 7 and 16 tokens (ragged 8-column units)
+    w = _wl("decode", n_seqs=n_seqs, seq_len=1, ctx=64, hidden=4096, n_heads=32, n_kv=8,
+            head_dim=128, inter=2048)
+    model, h, _ = _run_layer(w, 8, fused=True)
+    ref, _, _ = _oracle_layer(w)
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    # the unfused reduction (per-rank partials, then the ordered sum): same result
+    model2, h2, _ = _run_layer(w, 8, fused=False)
+    assert rel_err(to_f64(h2), to_f64(h)) <= 1e-2
+    model.close(); model2.close()
