@@ -469,7 +469,9 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
   const int64_t T = a.total_iters;  // stream-K iterations
   const int K = a.k_slices * a.k_iters_slice;  // K steps per tile
   const int64_t dp_tiles = (int64_t)a.dp_waves * G;
-  const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
+  const int Gs = a.sk_ctas > 0 ? a.sk_ctas : G;  // CTAs sharing the stream-K part
+  const int64_t beg = c < Gs ? range_begin(c, T, Gs) : T;
+  const int64_t end = c < Gs ? range_begin(c + 1, T, Gs) : T;
   auto make_iter = [&]() {
     SegIter si;
     si.G = G; si.c = c; si.K = K; si.W = a.dp_waves;
@@ -682,8 +684,8 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       int64_t ts = 0;
       if (sg.sk) {
         ts = sg.tile - dp_tiles;
-        c_first = owner_of(ts * K, T, G);
-        nseg = owner_of((ts + 1) * K - 1, T, G) - c_first + 1;
+        c_first = owner_of(ts * K, T, Gs);
+        nseg = owner_of((ts + 1) * K - 1, T, Gs) - c_first + 1;
       }
       if (nseg == 1) {
         if constexpr (SWAP) {
@@ -740,7 +742,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
           // piece then sits in slot 1).  Loads of up to 4 pieces are in flight
           // together, and the first batch of the next chunk is fetched before
           // the current chunk is stored.
-          const int slot0 = range_begin(c_first, T, G) == ts * K ? 0 : 1;
+          const int slot0 = range_begin(c_first, T, Gs) == ts * K ? 0 : 1;
           const float* base = a.partials + (int64_t)c_first * 2 * BN * 128 + row;
           float tmp[4][16];
           auto load_batch = [&](int c0, int s0) {

@@ -72,6 +72,8 @@ struct GemmArgs {
   int dp_waves;             // W: tiles [0, W*G) are whole-tile, data-parallel
   int cluster_split;        // s > 1: cluster of s CTAs per tile, K split s ways (DSMEM sum)
   int64_t total_iters;      // (n_tiles - W*G) * k_slices * k_iters_slice (stream-K part)
+  int sk_ctas;              // CTAs 0..sk_ctas-1 share the stream-K part (0: all G); with
+                            // sk_ctas = n_tiles - W*G each of them takes one whole tile
   float* partials;          // [G][2][BN][128]
   int* tickets;             // [n_tiles], zero on entry and exit
   int* status;              // device status word
