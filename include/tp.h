@@ -398,6 +398,15 @@ tp_status tp_profile_read(tp_model* m, void* stream, tp_kernel_time_t* out, int3
  * TP_ERR_TOKEN_RANGE or TP_ERR_DEVICE_TIMEOUT) and clears it. */
 tp_status tp_check_device(tp_model* m, void* stream);
 
+/* Failure-detection self-test (no counterpart on the pages): launches one
+ * warp that waits on an mbarrier phase nothing ever completes, through the
+ * same bounded wait every kernel of the library uses, with its limit set to
+ * about `milliseconds` (1..5000) of SM clock.  The wait gives up, records
+ * TP_ERR_DEVICE_TIMEOUT in the model's status word and the kernel returns;
+ * nothing faults and the context stays usable.  tp_check_device reports and
+ * clears the status. */
+tp_status tp_selftest_wait_timeout(tp_model* m, int32_t milliseconds, void* stream);
+
 const char* tp_strerror(tp_status s);
 
 #ifdef __cplusplus

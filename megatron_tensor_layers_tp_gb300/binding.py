@@ -108,6 +108,7 @@ _SIGS = {
     "tp_get_stats": (c_int32, [c_void_p, POINTER(tp_stats_t)]),
     "tp_reset_stats": (None, [c_void_p]),
     "tp_check_device": (c_int32, [c_void_p, c_void_p]),
+    "tp_selftest_wait_timeout": (c_int32, [c_void_p, c_int32, c_void_p]),
     "tp_strerror": (c_char_p, [c_int32]),
     "tp_profile": (c_int32, [c_void_p, c_int32]),
     "tp_profile_read": (c_int32, [c_void_p, c_void_p, POINTER(tp_kernel_time_t), c_int32,

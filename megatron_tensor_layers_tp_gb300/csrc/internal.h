@@ -171,5 +171,6 @@ cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st);
 cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, int t,
                               cudaStream_t st);
+cudaError_t launch_wait_timeout(int* status, long long limit, cudaStream_t st);
 
 }  // namespace tpk

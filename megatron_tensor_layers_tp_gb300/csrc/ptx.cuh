@@ -59,7 +59,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // (~2 s at the GB300 clock) have passed; the cycle counter is read only every
 // 64 failed polls.
 constexpr long long kWaitLimitCycles = 4000000000ll;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = -1;
   uint32_t n = 0;
@@ -69,7 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
       const long long now = clock64();
       if (t0 < 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitCycles) {
+      } else if (now - t0 > limit) {
         record_status(status, kStatusTimeout);
         return false;
       }

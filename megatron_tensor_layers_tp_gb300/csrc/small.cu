@@ -270,6 +270,26 @@ cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, 
   return launch_k(stage_send_kernel, dim3(M, t), dim3(128), 0, st, src, dst, H, H / t);
 }
 
+// ---------------------------------------------------------------------------
+// Failure-detection self-test: one warp waits on an mbarrier phase that no
+// arrival ever completes.  The bounded wait gives up after `limit` SM cycles,
+// records the timeout in *status and the kernel returns normally.
+// ---------------------------------------------------------------------------
+__global__ void wait_timeout_kernel(int* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, status, limit);  // phase 0 never completes
+}
+
+cudaError_t launch_wait_timeout(int* status, long long limit, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;

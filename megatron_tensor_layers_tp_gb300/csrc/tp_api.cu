@@ -1143,6 +1143,18 @@ void tp_reset_stats(tp_model* m) {
   if (m) memset(&m->stats, 0, sizeof(m->stats));
 }
 
+tp_status tp_selftest_wait_timeout(tp_model* m, int32_t milliseconds, void* stream) {
+  if (!m || milliseconds < 1 || milliseconds > 5000) return TP_ERR_ARG;
+  int dev = 0, khz = 0;
+  TP_CHECK_CUDA(cudaGetDevice(&dev));
+  TP_CHECK_CUDA(cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev));
+  const long long cycles = (long long)milliseconds * (khz > 0 ? khz : 2000000);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch(m, "wait_timeout", st, [&] {
+    return launch_wait_timeout(m->status, cycles, st);
+  }));
+}
+
 tp_status tp_check_device(tp_model* m, void* stream) {
   if (!m) return TP_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
