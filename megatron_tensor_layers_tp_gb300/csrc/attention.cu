@@ -189,6 +189,17 @@ struct DecSmem {
   }
 };
 
+// one output row slice of N fp32 values scaled by inv, stored as N bf16 (16 or 8 bytes)
+template <int N>
+__device__ __forceinline__ void store_out_row(uint16_t* dst, const float (&v)[N], float inv) {
+  static_assert(N == 8 || N == 4, "row slice of 8 or 4 columns");
+  uint32_t p[N / 2];
+#pragma unroll
+  for (int q = 0; q < N / 2; ++q) p[q] = pack2(v[2 * q] * inv, v[2 * q + 1] * inv);
+  if constexpr (N == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
+  else *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   using L = DecSmem<D>;
@@ -344,19 +355,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
-      // row = ct / 8, 16 columns each (D = 128) or 8 (D = 64); the second
-      // group's threads repeat the first group's arithmetic and store nothing
-      constexpr int CPT = D / 8;
-      const bool cthr = ctid < kDecGroupWarps * 32;
-      const int ct = ctid & (kDecGroupWarps * 32 - 1);
-      const int row = ct >> 3, c0 = (ct & 7) * CPT;
+      // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128)
+      constexpr int CPT = D / 16;
+      const int row = ctid >> 4, c0 = (ctid & 15) * CPT;
       float mm = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
       float ll = 0.f, acc[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
-#pragma unroll
+#pragma unroll 2
       for (int w = 0; w < kDecWarps; ++w) {
         const float* cr = comb + (w * 16 + row) * (D + 2);
         const float mw = cr[D];
@@ -369,26 +377,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
       uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + c0;
       if (nseg == 1) {
-        if (cthr && row < a.group) {
-          const float inv = 1.f / ll;
-#pragma unroll
-          for (int j = 0; j < CPT; j += 8) {
-            uint4 v;
-            uint32_t* p = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) p[q] = pack2(acc[j + 2 * q] * inv, acc[j + 2 * q + 1] * inv);
-            *reinterpret_cast<uint4*>(orow + j) = v;
-          }
-        }
+        if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
       } else {
         const int first_c = owner_of(bg * TB, T, G);
         const int my_slot = (beg / TB == bg) ? 0 : 1;
         float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
-        if (cthr) {
 #pragma unroll
-          for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
-          if ((ct & 7) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
-        }
+        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
+        if ((ctid & 15) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
         __threadfence();
         bar_sync(1, kDecWarps * 32);
         if (ctid == 0) {
@@ -419,18 +415,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + c0 + j]) * sc;
           }
-          if (cthr && row < a.group) {
-            const float inv = 1.f / L2;
-#pragma unroll
-            for (int j = 0; j < CPT; j += 8) {
-              uint4 v;
-              uint32_t* p = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                p[q] = pack2(acc2[j + 2 * q] * inv, acc2[j + 2 * q + 1] * inv);
-              *reinterpret_cast<uint4*>(orow + j) = v;
-            }
-          }
+          if (row < a.group) store_out_row<CPT>(orow, acc2, 1.f / L2);
           if (ctid == 0) a.tickets[bg] = 0;
         }
       }
