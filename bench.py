@@ -59,6 +59,9 @@ def parse():
 # ---------------------------------------------------------------------------
 # byte accounting (algorithmic: what the method must move once per step)
 # ---------------------------------------------------------------------------
+NORM_IN_GEMM_TOKENS = 32  # the library's decode-orientation RMSNorm fold limit
+
+
 def layer_bytes(w, t):
     H, d, I = w.hidden, w.head_dim, w.intermediate
     M = w.tokens
@@ -70,7 +73,11 @@ def layer_bytes(w, t):
         "attn_decode": w.n_seqs * w.n_kv_heads * w.ctx * d * 2 * 2 + 2 * M * w.n_heads * d * 2,
         "rmsnorm": 2 * M * H * 2 + H * 2,
     }
-    total = sum(b.values()) + b["rmsnorm"]  # two norms per layer
+    # two norms per layer; up to NORM_IN_GEMM_TOKENS tokens the library
+    # applies them inside qkv / gate_up (reading h, already counted there)
+    total = sum(b.values()) + b["rmsnorm"]
+    if M <= NORM_IN_GEMM_TOKENS:
+        total -= 2 * b["rmsnorm"]
     return b, total
 
 

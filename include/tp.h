@@ -144,7 +144,11 @@ typedef struct tp_model tp_model; /* opaque: owns the shard buffers */
  *   embed / lm_head shard r: vocab rows [r Vp/t, (r+1) Vp/t), zero padded
  * Within a shard, rows are stored in the order the fused epilogues want (the
  * two halves of each RoPE pair, and each gate row with its up row, sit next
- * to each other); every output of the API is in the standard order. */
+ * to each other); every output of the API is in the standard order.
+ * The decoder layer path also keeps a second copy of every qkv and gate_up
+ * shard with the preceding RMSNorm's weight folded into its columns
+ * (W[n][k] * w[k], rounded to bf16): (x / rms(x) * w) . W[n] equals
+ * (x . (W[n] * w)) / rms(x).  tp_column_linear uses the plain shards. */
 tp_status tp_load_shards(const tp_config_t* cfg, const tp_weights_t* w, void* stream,
                          tp_model** out);
 void tp_free(tp_model* m);
@@ -252,7 +256,11 @@ typedef struct {
  *   a = SiLU(gate) * up from column-parallel gate_up_proj(u)
  *   h = h + all_reduce(row-parallel down_proj(a))        reduction ②
  * h_inout [n_tokens, H] bf16 is read and overwritten.  fused selects the
- * row-parallel reduction variant (see tp_row_linear_reduce). */
+ * row-parallel reduction variant (see tp_row_linear_reduce).
+ * Each RMSNorm's weight is folded into the GEMM after it (tp_load_shards).
+ * Up to 32 tokens that GEMM reads h and scales token m's outputs by
+ * 1/sqrt(mean(h_m^2) + eps), computed in fp32 inside it (five kernels per
+ * layer); above 32 a norm kernel writes h / rms(h) first (seven). */
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
                            tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
                            void* stream);

@@ -93,6 +93,10 @@ constexpr int kThreadsOf = (2 + kEpiWarps<SWAP>) * 32;
 
 template <int EPI>
 constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || EPI == EPI_RESID;
+// Epilogues that can scale by a folded RMSNorm's 1/rms (decode orientation):
+// the two column-parallel GEMMs that follow a norm in the decoder layer.
+template <int EPI>
+constexpr bool kEpiNorm = EPI == EPI_QKV || EPI == EPI_SILU;
 // Multi-chunk epilogues fetch the next chunk's inputs before storing the
 // current one, except qkv, whose inputs (positions, RoPE factors) would not
 // fit in registers twice next to the fix-up's pieces.
@@ -168,6 +172,13 @@ template <bool SWAP, int EPI>
 __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
                                           const int* tok, float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
+  if constexpr (SWAP && kEpiNorm<EPI>) {
+    if (e.norm_src) {  // the token's 1/rms, staged in shared memory after tok
+      const float* rs = reinterpret_cast<const float*>(tok + 4 * kSwapMaxTokens);
+#pragma unroll
+      for (int j = 0; j < kUnit<SWAP>; ++j) v[j] *= rs[brow0 + j];
+    }
+  }
   if constexpr (kEpiBias<EPI>) {
     if (e.bias) {  // before RoPE / SiLU pairing and the residual
 #pragma unroll
@@ -446,6 +457,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* tok = reinterpret_cast<int*>(last_flag + 3);  // decode: positions, sequences, cache offsets
+  // then (decode, folded RMSNorm) kSwapMaxTokens floats: each token's 1/rms
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -613,6 +625,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       if constexpr (SWAP) tmem_ld8(addr, v);
       else tmem_ld16(addr, v);
     };
+    bool staged = false;
     if constexpr (SWAP && EPI == EPI_QKV) {
       // every tile of the decode orientation covers tokens 0..M-1
       if (et < kSwapMaxTokens) {
@@ -624,8 +637,45 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
         reinterpret_cast<int64_t*>(tok + 2 * kSwapMaxTokens)[et] =
             ((int64_t)seq * a.e.kv_heads_per_rank * a.e.l_max + pos) * a.e.head_dim;
       }
-      bar_sync(1, ET);
+      staged = true;
     }
+    if constexpr (SWAP && kEpiNorm<EPI>) {
+      if (a.e.norm_src) {
+        // the folded RMSNorm's 1/rms of every token, one warp per token, while
+        // the MMA warp streams the weights (the hidden rows come from L2)
+        float* rs = reinterpret_cast<float*>(tok + 4 * kSwapMaxTokens);
+        const int ew = et >> 5, nv = a.e.norm_width >> 3;
+        for (int m = ew; m < a.e.M; m += kEpiWarps<SWAP>) {
+          const uint4* xr = reinterpret_cast<const uint4*>(a.e.norm_src + (int64_t)m * a.e.norm_ld);
+          float ss = 0.f;
+          auto add_sq = [&](const uint4& p) {
+            const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+              ss = fmaf(lo, lo, ss);
+              ss = fmaf(hi, hi, ss);
+            }
+          };
+          // eight independent 16-byte loads in flight per lane, then their squares
+          int v = lane;
+          for (; v + 7 * 32 < nv; v += 8 * 32) {
+            uint4 p[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) p[q] = __ldcg(xr + v + q * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) add_sq(p[q]);
+          }
+          for (; v < nv; v += 32) add_sq(__ldcg(xr + v));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          if (lane == 0) rs[m] = 1.0f / sqrtf(ss / (float)a.e.norm_width + a.e.norm_eps);
+        }
+        if (et >= a.e.M && et < kSwapMaxTokens) rs[et] = 0.f;
+        staged = true;
+      }
+    }
+    if (staged) bar_sync(1, ET);
     // units this thread stores itself: columns c0 = u0, u0 + ustep, ... of a
     // tile; in a cluster split the (half, rank) workers of the cluster share
     // the units of the one tile

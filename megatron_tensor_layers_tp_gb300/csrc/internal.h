@@ -50,6 +50,15 @@ struct EpiArgs {
   // value of output row f of rank g is bias[g * bias_group_stride + f]
   const uint16_t* bias;
   int64_t bias_group_stride;
+  // RMSNorm folded into the GEMM (decode orientation, QKV and SILU): the
+  // weights already carry the norm weight w (W[n][k] * w[k], rounded to bf16
+  // at load) and the GEMM reads the raw hidden state, so every output of
+  // token m is scaled by 1 / sqrt(mean_k norm_src[m][k]^2 + norm_eps) before
+  // bias, RoPE and SiLU.  norm_src == nullptr: no scaling.
+  const uint16_t* norm_src;
+  int64_t norm_ld;          // row stride of norm_src (elements)
+  int norm_width;           // k extent (H), a multiple of 8
+  float norm_eps;
 };
 
 struct GemmArgs {
@@ -167,6 +176,11 @@ cudaError_t launch_reduce_ranks(const float* partials, int64_t rank_stride, int 
                                 cudaStream_t st);
 cudaError_t launch_rope_table(float2* table, int max_pos, int head_dim, double theta,
                               cudaStream_t st);
+// dst[i][k] = bf16(src[i][k] * w[k]) for n_rows rows of cols elements (RNE;
+// the fp32 product of two bf16 values is exact).  Folds an RMSNorm weight into
+// the weight rows that consume its output.
+cudaError_t launch_fold_cols(uint16_t* dst, const uint16_t* src, const uint16_t* w, int64_t n_rows,
+                             int cols, cudaStream_t st);
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st);
 cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, int t,

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <algorithm>
 #include <stdint.h>
 
 #include "internal.h"
@@ -287,6 +289,29 @@ __global__ void wait_timeout_kernel(int* status, long long limit) {
 
 cudaError_t launch_wait_timeout(int* status, long long limit, cudaStream_t st) {
   wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm weight folded into the rows of the GEMM that consumes the norm's
+// output (load time): (x / rms(x) * w) . W[n] = (x . (W[n] * w)) / rms(x), so
+// W[n][k] * w[k] is stored once and the per-token 1/rms is applied to the
+// GEMM's output.  One thread per element; fp32 product (exact for two bf16
+// values), rounded to nearest even.
+// ---------------------------------------------------------------------------
+__global__ void fold_cols_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
+                                 const uint16_t* __restrict__ w, int64_t n, int cols) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = f_to_bf16(bf16_to_f(src[i]) * bf16_to_f(w[i % cols]));
+}
+
+cudaError_t launch_fold_cols(uint16_t* dst, const uint16_t* src, const uint16_t* w, int64_t n_rows,
+                             int cols, cudaStream_t st) {
+  const int64_t n = n_rows * cols;
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 1 << 20);
+  fold_cols_kernel<<<(unsigned)blocks, 256, 0, st>>>(dst, src, w, n, cols);
   return cudaGetLastError();
 }
 

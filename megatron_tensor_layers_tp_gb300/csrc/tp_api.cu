@@ -27,6 +27,10 @@ struct ShardedLinear {
 
 struct LayerShards {
   ShardedLinear qkv, gate_up, o, down;
+  // qkv and gate_up with the preceding RMSNorm's weight folded into their
+  // columns (W[n][k] * w[k]): the decoder layer's GEMMs read these, and the
+  // raw hidden state; tp_column_linear keeps the plain shards
+  ShardedLinear qkv_folded, gate_up_folded;
   uint16_t* attn_norm = nullptr;
   uint16_t* mlp_norm = nullptr;
 };
@@ -39,6 +43,7 @@ struct tp_model {
   uint16_t* embed = nullptr;  // [Vp][H] = t shards of [Vp/t][H]
   ShardedLinear lm;
   uint16_t* final_norm = nullptr;
+  uint16_t* ones = nullptr;  // [H] bf16 1.0: the norm weight once it is folded
   float2* rope = nullptr;
   int* status = nullptr;
   std::vector<void*> allocs;
@@ -54,6 +59,7 @@ struct tp_model {
 namespace {
 
 constexpr int kPrefillBN = 256;
+constexpr int kNormInGemmTokens = 32;  // folded RMSNorm applied inside the GEMM up to here
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -165,7 +171,7 @@ GemmPlan plan_gemm(int M) {
   int cols = 32;
   while (cols < 2 * p.BN) cols *= 2;
   p.tmem_cols = cols;
-  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 4 * kSwapMaxTokens * 4;
+  p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 5 * kSwapMaxTokens * 4;
   return p;
 }
 
@@ -732,6 +738,23 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
         cudaMemcpyAsync(Ls.mlp_norm, Wl.mlp_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) !=
             cudaSuccess)
       return fail(TP_ERR_CUDA);
+    // the norms' weights folded into the column-parallel GEMMs that read them
+    if ((s = alloc_linear(m, &Ls.qkv_folded, nqkv, H, at)) != TP_OK ||
+        (s = alloc_linear(m, &Ls.gate_up_folded, 2 * Ipr, H, t)) != TP_OK)
+      return fail(s);
+    Ls.qkv_folded.bias = Ls.qkv.bias;
+    Ls.gate_up_folded.bias = Ls.gate_up.bias;
+    if (launch_fold_cols(Ls.qkv_folded.data, Ls.qkv.data, Ls.attn_norm, (int64_t)at * nqkv, H, st) !=
+            cudaSuccess ||
+        launch_fold_cols(Ls.gate_up_folded.data, Ls.gate_up.data, Ls.mlp_norm, (int64_t)t * 2 * Ipr,
+                         H, st) != cudaSuccess)
+      return fail(TP_ERR_CUDA);
+  }
+  {
+    const std::vector<uint16_t> one(H, 0x3F80);  // bf16 1.0
+    if ((s = dev_alloc(m, &m->ones, (size_t)H * 2)) != TP_OK) return fail(s);
+    if (cudaMemcpyAsync(m->ones, one.data(), (size_t)H * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return fail(TP_ERR_CUDA);
   }
   // vocab-parallel tables: padded to Vp rows, shard r = rows [r Vp/t, (r+1) Vp/t)
   if (w->embed || w->lm_head) {
@@ -880,12 +903,29 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   uint16_t* vc = b->v_cache[layer];
   if (!kc || !vc || !aligned16(kc) || !aligned16(vc)) return TP_ERR_ARG;
   tp_status s;
-  // u = RMSNorm(h)
-  TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
-    return launch_rmsnorm(h, H, nullptr, Ls.attn_norm, M, H, c.rms_eps, u, H, st, true);
-  }));
+  // Each RMSNorm's weight is folded into the GEMM after it (qkv_folded,
+  // gate_up_folded).  Up to kNormInGemmTokens tokens that GEMM reads h itself
+  // and scales each token's outputs by its 1/rms, computed by its epilogue
+  // warps while the weights stream (every CTA reads all M rows of h from L2:
+  // measured a net gain at 16 tokens, a loss at 64, where those reads outgrow
+  // a CTA's share of the qkv weights).  Otherwise u = h / rms(h) first.
+  const bool fold = plan_gemm(M).swap && M <= kNormInGemmTokens;
+  auto norm_in = [&](EpiArgs& e_) -> tp_status {
+    if (fold) {
+      e_.norm_src = h;
+      e_.norm_ld = H;
+      e_.norm_width = H;
+      e_.norm_eps = c.rms_eps;
+      return TP_OK;
+    }
+    return cuda_status(launch(m, "rmsnorm", st, [&] {
+      return launch_rmsnorm(h, H, nullptr, m->ones, M, H, c.rms_eps, u, H, st, true);
+    }));
+  };
+  const uint16_t* xin = fold ? h : u;
   // qkv (column-parallel) + RoPE + K/V into the rank caches
   EpiArgs e = base_epi(m, M);
+  if ((s = norm_in(e)) != TP_OK) return s;
   e.out = q;
   e.ld_out = nhd;
   e.k_cache = kc;
@@ -896,7 +936,8 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   e.positions = b->positions;
   e.token_seq = b->token_seq;
   e.rope = m->rope;
-  if ((s = run_column(m, "gemm_qkv", Ls.qkv, u, H, M, EPI_QKV, e, ws, L, st)) != TP_OK) return s;
+  if ((s = run_column(m, "gemm_qkv", Ls.qkv_folded, xin, H, M, EPI_QKV, e, ws, L, st)) != TP_OK)
+    return s;
   // attention
   AttnArgs a;
   memset(&a, 0, sizeof(a));
@@ -952,14 +993,14 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
     m->stats.dp_gathers++;
     m->stats.dp_gather_recv_bytes_per_rank += (int64_t)(c.attn_dp - 1) * M * H * 2 / c.attn_dp;
   }
-  // u = RMSNorm(h); gate_up (column-parallel) + SiLU(gate) * up
-  TP_CHECK_CUDA(launch(m, "rmsnorm", st, [&] {
-    return launch_rmsnorm(h, H, nullptr, Ls.mlp_norm, M, H, c.rms_eps, u, H, st, true);
-  }));
+  // RMSNorm(h) folded as above; gate_up (column-parallel) + SiLU(gate) * up
   EpiArgs e2 = base_epi(m, M);
+  if ((s = norm_in(e2)) != TP_OK) return s;
   e2.out = act;
   e2.ld_out = c.intermediate;
-  if ((s = run_column(m, "gemm_gate_up", Ls.gate_up, u, H, M, EPI_SILU, e2, ws, L, st)) != TP_OK) return s;
+  if ((s = run_column(m, "gemm_gate_up", Ls.gate_up_folded, xin, H, M, EPI_SILU, e2, ws, L, st)) !=
+      TP_OK)
+    return s;
   // down_proj (row-parallel) + reduction ② + residual
   return run_row(m, "gemm_down", Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws, L, st);
 }

@@ -107,6 +107,53 @@ def test_ragged_prefill_matches_oracle():
     model.close()
 
 
+def _ragged_prefill(w, t, lens, seed):
+    model, _, _ = build_model(w, t, max_tokens=sum(lens))
+    n = len(lens)
+    ks = [model.alloc_kv(n, w.ctx)]
+    vs = [model.alloc_kv(n, w.ctx)]
+    from tests.parity_utils import fill_device_kv
+    fill_device_kv(model, w, ks[0], "k_cache", 0)
+    fill_device_kv(model, w, vs[0], "v_cache", 0)
+    pos = np.concatenate([np.arange(k) for k in lens]).astype(np.int32)
+    seq = np.concatenate([np.full(k, b) for b, k in enumerate(lens)]).astype(np.int32)
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    M = sum(lens)
+    batch = Batch(B.TP_PREFILL, n, M, max(lens), max(lens), w.ctx, torch.from_numpy(pos).cuda(),
+                  torch.from_numpy(seq).cuda(), torch.from_numpy(start).cuda(), ks, vs, None)
+    hx = synth.normal_f64(seed, 555, (M, w.hidden), 1.0)
+    h = torch.from_numpy(hx.astype(np.float32)).to(torch.bfloat16).cuda()
+    model.reset_stats()
+    model.layer_forward(0, batch, h)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    launches = model.stats().kernel_launches
+    kc, vc = oracle_caches(w, 0, range(n))
+    ref = O.layer_forward(hx, oracle_layer(w, 0), kc, vc, O.Batch(seq, pos), oracle_dims(w))
+    err = rel_err(to_f64(h), ref)
+    model.close()
+    return err, launches
+
+
+@pytest.mark.parametrize("t", [1, 4])
+def test_short_prefill_with_norm_inside_the_gemms_matches_oracle(t):
+    # 27 tokens: the decode orientation, RMSNorm folded into qkv / gate_up,
+    # causal prefill attention over ragged sequences
+    w = _wl("prefill", n_seqs=3, seq_len=16, ctx=16)
+    err, launches = _ragged_prefill(w, t, [3, 16, 8], 6)
+    assert err <= LAYER_TOL
+    assert launches == 5  # qkv, attention, o_proj, gate_up, down_proj: no norm kernel
+
+
+def test_norm_kernels_return_above_32_tokens():
+    # 48 tokens: the RMSNorms run as kernels (unit weight; the norm weights are
+    # folded into qkv / gate_up either way)
+    w = _wl("prefill", n_seqs=3, seq_len=16, ctx=16)
+    err, launches = _ragged_prefill(w, 2, [16, 16, 16], 7)
+    assert err <= LAYER_TOL
+    assert launches == 7
+
+
 def test_sharded_equals_unsharded_on_gpu():
     w = _wl("decode", n_seqs=16, seq_len=1, ctx=300, hidden=1024, n_heads=16, n_kv=8, head_dim=64,
             inter=2048)
@@ -184,10 +231,11 @@ def test_two_layer_forward_with_padded_vocab_and_counters():
     model.close()
 
 
-@pytest.mark.parametrize("n_seqs", [1, 7, 16])
+@pytest.mark.parametrize("n_seqs", [1, 7, 16, 40])
 def test_decode_layer_4096_wide_ragged_tokens_matches_oracle(n_seqs):
     # hidden 4096: o_proj and down_proj run as 32 clusters of 4 CTAs, qkv and
-    # gate_up as stream-K, at 1, 7 and 16 tokens (ragged 8-column units)
+    # gate_up as stream-K, at 1, 7 and 16 tokens (ragged 8-column units; the
+    # RMSNorms applied inside qkv / gate_up) and 40 (RMSNorm kernels first)
     w = _wl("decode", n_seqs=n_seqs, seq_len=1, ctx=64, hidden=4096, n_heads=32, n_kv=8,
             head_dim=128, inter=2048)
     model, h, _ = _run_layer(w, 8, fused=True)
