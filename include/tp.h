@@ -260,7 +260,10 @@ typedef struct {
  * Each RMSNorm's weight is folded into the GEMM after it (tp_load_shards).
  * Up to 32 tokens that GEMM reads h and scales token m's outputs by
  * 1/sqrt(mean(h_m^2) + eps), computed in fp32 inside it (five kernels per
- * layer); above 32 a norm kernel writes h / rms(h) first (seven). */
+ * layer).  Above 32 tokens (up to 64) the second norm takes its sums of
+ * squares from o_proj (fused reduction), and in tp_forward / tp_stage_forward
+ * so does every later layer's first norm (from down_proj); the first norm of
+ * the call runs as a kernel. */
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
                            tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
                            void* stream);

@@ -91,8 +91,11 @@ constexpr int kEpiWarps = SWAP ? 8 : 4;
 template <bool SWAP>
 constexpr int kThreadsOf = (2 + kEpiWarps<SWAP>) * 32;
 
+// the fused row-parallel epilogues: residual + rank sum (+ the next norm's sums of squares)
 template <int EPI>
-constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || EPI == EPI_RESID;
+constexpr bool kResid = EPI == EPI_RESID || EPI == EPI_RESID_SQ;
+template <int EPI>
+constexpr bool kEpiBias = EPI == EPI_PLAIN || EPI == EPI_QKV || EPI == EPI_SILU || kResid<EPI>;
 // Epilogues that can scale by a folded RMSNorm's 1/rms (decode orientation):
 // the two column-parallel GEMMs that follow a norm in the decoder layer.
 template <int EPI>
@@ -121,7 +124,7 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
       }
     }
   }
-  if constexpr (SWAP && EPI == EPI_RESID) {
+  if constexpr (SWAP && kResid<EPI>) {
 #pragma unroll
     for (int j = 0; j < kUnit<SWAP>; ++j) {
       const int m = brow0 + j;
@@ -142,7 +145,7 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
       const bool ok = in.pos[j] >= 0 && in.pos[j] < e.l_max;
       in.cs[j] = (ok && kind != 2) ? e.rope[(int64_t)in.pos[j] * half + jp] : make_float2(1.f, 0.f);
     }
-  } else if constexpr (!SWAP && EPI == EPI_RESID) {
+  } else if constexpr (!SWAP && kResid<EPI>) {
     // prefill orientation: lane = token m, 16 consecutive features f0..f0+15
     const int m = arow, f0 = brow0;
     if (e.residual && m < e.M && f0 < a.b_rows_valid) {
@@ -173,7 +176,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
                                           const int* tok, float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
   if constexpr (SWAP && kEpiNorm<EPI>) {
-    if (e.norm_src) {  // the token's 1/rms, staged in shared memory after tok
+    if (e.norm_mode) {  // the token's 1/rms, staged in shared memory after tok
       const float* rs = reinterpret_cast<const float*>(tok + 4 * kSwapMaxTokens);
 #pragma unroll
       for (int j = 0; j < kUnit<SWAP>; ++j) v[j] *= rs[brow0 + j];
@@ -198,6 +201,35 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
         const int m = brow0 + j;
         if (fval && m < e.M) out[(int64_t)m * e.ld_out + f] = f_to_bf16(v[j] + in.r[j]);
       }
+    } else if constexpr (EPI == EPI_RESID_SQ) {
+      uint16_t* out = static_cast<uint16_t*>(e.out);
+      float sq[kUnit<SWAP>];
+#pragma unroll
+      for (int j = 0; j < kUnit<SWAP>; ++j) {
+        const int m = brow0 + j;
+        const uint16_t ob = f_to_bf16(v[j] + in.r[j]);
+        const bool st = fval && m < e.M;
+        if (st) out[(int64_t)m * e.ld_out + f] = ob;
+        const float of = bf16_to_f(ob);
+        sq[j] = st ? of * of : 0.f;
+      }
+      // the next RMSNorm's sums of squares over this warp's 32 features, per
+      // token: halve the token set at each exchange (xor 16, 8, 4), then
+      // finish the sum over lane bits 1 and 0; lane 4j ends with token j
+      static_assert(kUnit<SWAP> == 8, "8 tokens per unit");
+      const int lane = threadIdx.x & 31;
+      float s4[4], s2[2];
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        s4[i] = (b4 ? sq[4 + i] : sq[i]) + __shfl_xor_sync(0xffffffffu, b4 ? sq[i] : sq[4 + i], 16);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        s2[i] = (b3 ? s4[2 + i] : s4[i]) + __shfl_xor_sync(0xffffffffu, b3 ? s4[i] : s4[2 + i], 8);
+      float s1 = (b2 ? s2[1] : s2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? s2[0] : s2[1], 4);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      if ((lane & 3) == 0) e.sq_out[(int64_t)(brow0 + (lane >> 2)) * e.sq_ld + (f >> 5)] = s1;
     } else if constexpr (EPI == EPI_PARTIAL) {
       float* out = static_cast<float*>(e.out) + (int64_t)g * e.out_group_stride;
 #pragma unroll
@@ -273,7 +305,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
     const int m = arow;
     const int f0 = brow0;
     if (m >= e.M || f0 >= a.b_rows_valid) return;
-    if constexpr (EPI == EPI_RESID) {
+    if constexpr (kResid<EPI>) {
       uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out + f0;
       const float* r = in.r;
       uint4 o0, o1;
@@ -640,7 +672,40 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       staged = true;
     }
     if constexpr (SWAP && kEpiNorm<EPI>) {
-      if (a.e.norm_src) {
+      if (a.e.norm_mode == 2) {
+        // the folded RMSNorm's 1/rms of every token from the sums of squares
+        // the kernel that wrote h left behind (fixed order: deterministic)
+        // (the warp's tokens m = ew + 8 q: one 16-byte load per lane and token,
+        // all tokens' loads in flight together)
+        float* rs = reinterpret_cast<float*>(tok + 4 * kSwapMaxTokens);
+        const int ew = et >> 5, n4 = a.e.norm_slots >> 2;
+        constexpr int QW = kSwapMaxTokens / kEpiWarps<SWAP>;
+        float ss[QW];
+#pragma unroll
+        for (int q = 0; q < QW; ++q) ss[q] = 0.f;
+        for (int i4 = lane; i4 < n4; i4 += 32) {
+          float4 p[QW];
+#pragma unroll
+          for (int q = 0; q < QW; ++q) {
+            const int m = ew + q * kEpiWarps<SWAP>;
+            p[q] = m < a.e.M ? __ldcg(reinterpret_cast<const float4*>(
+                                   a.e.norm_partials + (int64_t)m * a.e.norm_slots) + i4)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int q = 0; q < QW; ++q) ss[q] += (p[q].x + p[q].y) + (p[q].z + p[q].w);
+        }
+#pragma unroll
+        for (int q = 0; q < QW; ++q) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss[q] += __shfl_xor_sync(0xffffffffu, ss[q], o);
+          const int m = ew + q * kEpiWarps<SWAP>;
+          if (lane == 0 && m < a.e.M)
+            rs[m] = 1.0f / sqrtf(ss[q] / (float)a.e.norm_width + a.e.norm_eps);
+        }
+        if (et >= a.e.M && et < kSwapMaxTokens) rs[et] = 0.f;
+        staged = true;
+      } else if (a.e.norm_mode == 1) {
         // the folded RMSNorm's 1/rms of every token, one warp per token, while
         // the MMA warp streams the weights (the hidden rows come from L2)
         float* rs = reinterpret_cast<float*>(tok + 4 * kSwapMaxTokens);

@@ -19,6 +19,8 @@ enum Epi : int {
   EPI_RESID = 3,    // fused row-parallel: y = residual + sum of rank partials
   EPI_PARTIAL = 4,  // unfused row-parallel: fp32 partial of each rank
   EPI_LOGITS = 5,   // LM head: logits placed in the rank's vocab slot
+  EPI_RESID_SQ = 6, // EPI_RESID (decode orientation) that also leaves the next
+                    // RMSNorm's sums of squares (EpiArgs::sq_out)
 };
 
 struct EpiArgs {
@@ -53,12 +55,24 @@ struct EpiArgs {
   // RMSNorm folded into the GEMM (decode orientation, QKV and SILU): the
   // weights already carry the norm weight w (W[n][k] * w[k], rounded to bf16
   // at load) and the GEMM reads the raw hidden state, so every output of
-  // token m is scaled by 1 / sqrt(mean_k norm_src[m][k]^2 + norm_eps) before
-  // bias, RoPE and SiLU.  norm_src == nullptr: no scaling.
+  // token m is scaled by 1 / sqrt(ss_m / norm_width + norm_eps) before bias,
+  // RoPE and SiLU, where ss_m = sum_k h[m][k]^2 comes from
+  //   norm_mode 1: the rows of norm_src (read by the epilogue warps),
+  //   norm_mode 2: sum over i < norm_slots of norm_partials[m * norm_slots + i],
+  //                left by the kernel that wrote h (sq_out below);
+  //   norm_mode 0: no scaling.
+  int norm_mode;
   const uint16_t* norm_src;
   int64_t norm_ld;          // row stride of norm_src (elements)
   int norm_width;           // k extent (H), a multiple of 8
   float norm_eps;
+  const float* norm_partials;  // 16-byte aligned
+  int norm_slots;               // a multiple of 4
+  // EPI_RESID_SQ (decode orientation): the warp holding output features
+  // [32 i, 32 i + 32) for token m writes sq_out[m * sq_ld + i] = sum of the
+  // squares of those features' stored (bf16) values
+  float* sq_out;
+  int sq_ld;
 };
 
 struct GemmArgs {
@@ -155,6 +169,7 @@ TPK_DECLARE_EPI(2)
 TPK_DECLARE_EPI(3)
 TPK_DECLARE_EPI(4)
 TPK_DECLARE_EPI(5)
+TPK_DECLARE_EPI(6)
 
 // attention.cu
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);

@@ -225,8 +225,12 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
 // Workspace regions (all offsets 256-byte aligned).
 struct WsLayout {
   size_t gemm_tickets, attn_tickets, gemm_partials, attn_partials, u, q, o, act, hs, rank_partials,
-      total;
+      norm_sq, total;
 };
+
+// slots of per-32-feature sums of squares a row-parallel GEMM leaves for the
+// next RMSNorm (decode orientation): 4 per 128-row output tile
+int norm_slots(const tp_config_t& c) { return cdiv(c.hidden, 128) * 4; }
 
 size_t max_gemm_tiles(const tp_config_t& c, int M) {
   // upper bound over every GEMM of the model for M tokens
@@ -263,6 +267,7 @@ WsLayout ws_layout(const tp_model* m, int M) {
   L.act = take((size_t)M * c.intermediate * 2);
   L.hs = take((size_t)M * c.hidden * 2);
   L.rank_partials = take((size_t)c.t * M * c.hidden * sizeof(float));
+  L.norm_sq = take((size_t)kSwapMaxTokens * norm_slots(c) * sizeof(float));  // [token][slot]
   L.total = off;
   return L;
 }
@@ -345,7 +350,8 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
 // otherwise per-rank fp32 partials then the ordered reduction kernel.
 tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, const uint16_t* x,
                   int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
-                  uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st) {
+                  uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st,
+                  float* sq_out = nullptr) {
   if (M == 0) return TP_OK;
   const tp_config_t& c = m->cfg;
   const int Kr = W.cols, H = W.rows, t = W.ranks;
@@ -393,7 +399,9 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
     a.e.ld_res = H;
     a.e.bias = W.bias;  // once: the ranks are already summed in the accumulator
     a.e.bias_group_stride = 0;
-    epi = EPI_RESID;
+    a.e.sq_out = p.swap ? sq_out : nullptr;  // sums of squares for the next RMSNorm
+    a.e.sq_ld = norm_slots(c);
+    epi = a.e.sq_out ? EPI_RESID_SQ : EPI_RESID;
   } else {
     a.n_groups = t;
     a.k_slices = 1;
@@ -474,6 +482,7 @@ int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem) {
     case 3: n = gemm_max_clusters_epi3(swap, cluster_x, smem); break;
     case 4: n = gemm_max_clusters_epi4(swap, cluster_x, smem); break;
     case 5: n = gemm_max_clusters_epi5(swap, cluster_x, smem); break;
+    case 6: n = gemm_max_clusters_epi6(swap, cluster_x, smem); break;
   }
   cache.push_back({key, n});
   return n;
@@ -487,6 +496,7 @@ cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cuda
     case 3: return launch_gemm_epi3(swap, a, smem, st);
     case 4: return launch_gemm_epi4(swap, a, smem, st);
     case 5: return launch_gemm_epi5(swap, a, smem, st);
+    case 6: return launch_gemm_epi6(swap, a, smem, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -889,8 +899,12 @@ static tp_status check_batch(const tp_model* m, const tp_batch_t* b) {
   return TP_OK;
 }
 
+// h_sq: on entry, whether the sums of squares of h's rows sit in the
+// workspace (the previous layer's down_proj left them); on exit, whether this
+// layer's down_proj left them for the next.
 static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b, uint16_t* h,
-                               int fused, void* ws, const WsLayout& L, cudaStream_t st) {
+                               int fused, void* ws, const WsLayout& L, cudaStream_t st,
+                               bool* h_sq) {
   const tp_config_t& c = m->cfg;
   const LayerShards& Ls = m->layers[layer];
   const int M = b->n_tokens, H = c.hidden, d = c.head_dim;
@@ -904,28 +918,39 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   if (!kc || !vc || !aligned16(kc) || !aligned16(vc)) return TP_ERR_ARG;
   tp_status s;
   // Each RMSNorm's weight is folded into the GEMM after it (qkv_folded,
-  // gate_up_folded).  Up to kNormInGemmTokens tokens that GEMM reads h itself
-  // and scales each token's outputs by its 1/rms, computed by its epilogue
-  // warps while the weights stream (every CTA reads all M rows of h from L2:
-  // measured a net gain at 16 tokens, a loss at 64, where those reads outgrow
-  // a CTA's share of the qkv weights).  Otherwise u = h / rms(h) first.
-  const bool fold = plan_gemm(M).swap && M <= kNormInGemmTokens;
-  auto norm_in = [&](EpiArgs& e_) -> tp_status {
-    if (fold) {
-      e_.norm_src = h;
-      e_.norm_ld = H;
-      e_.norm_width = H;
-      e_.norm_eps = c.rms_eps;
-      return TP_OK;
-    }
+  // gate_up_folded).  In the decode orientation that GEMM reads h itself and
+  // scales each token's outputs by its 1/rms, which its epilogue warps get
+  // while the weights stream:
+  //  - up to kNormInGemmTokens tokens by reading h's rows (every CTA reads
+  //    all M rows from L2);
+  //  - above that from the sums of squares the fused row-parallel GEMM that
+  //    wrote h left in the workspace (measured: a ~1 us loss at 16 tokens
+  //    from the extra epilogue work in o_proj / down_proj, a gain at 64);
+  //  - otherwise (the layer's first norm without such sums, the unfused
+  //    reduction) u = h / rms(h) runs first.
+  const bool swap = plan_gemm(M).swap;
+  const bool leaves_sq = swap && fused != 0 && M > kNormInGemmTokens;  // o_proj, down_proj
+  float* sq = at<float>(ws, L.norm_sq);
+  auto norm_in = [&](EpiArgs& e_, bool have_sq, const uint16_t** xin) -> tp_status {
+    e_.norm_src = h;
+    e_.norm_ld = H;
+    e_.norm_width = H;
+    e_.norm_eps = c.rms_eps;
+    e_.norm_partials = sq;
+    e_.norm_slots = norm_slots(c);
+    *xin = h;
+    if (swap && M <= kNormInGemmTokens) { e_.norm_mode = 1; return TP_OK; }
+    if (swap && have_sq) { e_.norm_mode = 2; return TP_OK; }
+    e_.norm_mode = 0;
+    *xin = u;
     return cuda_status(launch(m, "rmsnorm", st, [&] {
       return launch_rmsnorm(h, H, nullptr, m->ones, M, H, c.rms_eps, u, H, st, true);
     }));
   };
-  const uint16_t* xin = fold ? h : u;
+  const uint16_t* xin = nullptr;
   // qkv (column-parallel) + RoPE + K/V into the rank caches
   EpiArgs e = base_epi(m, M);
-  if ((s = norm_in(e)) != TP_OK) return s;
+  if ((s = norm_in(e, *h_sq, &xin)) != TP_OK) return s;
   e.out = q;
   e.ld_out = nhd;
   e.k_cache = kc;
@@ -985,7 +1010,8 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
     TP_CHECK_CUDA(launch(m, "attn_prefill", st, [&] { return launch_attn_prefill(a, nqb, st); }));
   }
   // o_proj (row-parallel) + reduction ① + residual
-  if ((s = run_row(m, "gemm_o", Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st)) != TP_OK)
+  if ((s = run_row(m, "gemm_o", Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st,
+                   leaves_sq ? sq : nullptr)) != TP_OK)
     return s;
   // DP attention: every group's hidden rows are gathered for the MLP (one
   // buffer here; counted as each rank receiving the other groups' rows)
@@ -995,14 +1021,16 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   }
   // RMSNorm(h) folded as above; gate_up (column-parallel) + SiLU(gate) * up
   EpiArgs e2 = base_epi(m, M);
-  if ((s = norm_in(e2)) != TP_OK) return s;
+  if ((s = norm_in(e2, leaves_sq, &xin)) != TP_OK) return s;
   e2.out = act;
   e2.ld_out = c.intermediate;
   if ((s = run_column(m, "gemm_gate_up", Ls.gate_up_folded, xin, H, M, EPI_SILU, e2, ws, L, st)) !=
       TP_OK)
     return s;
   // down_proj (row-parallel) + reduction ② + residual
-  return run_row(m, "gemm_down", Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws, L, st);
+  *h_sq = leaves_sq;
+  return run_row(m, "gemm_down", Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws,
+                 L, st, leaves_sq ? sq : nullptr);
 }
 
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
@@ -1012,8 +1040,9 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
   tp_status s = check_batch(m, b);
   if (s != TP_OK) return s;
   if (!ws_ok(m, b->n_tokens, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  bool h_sq = false;  // the caller's h comes without sums of squares
   return layer_forward(m, layer, b, h_inout, fused, ws, ws_layout(m, b->n_tokens),
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), &h_sq);
 }
 
 // Layers [first, first + n) on h; the embedding first when ids is set, the
@@ -1036,8 +1065,9 @@ static tp_status stage_forward(const tp_model* m, int first, int n, const int32_
   const WsLayout L = ws_layout(m, rows);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (ids && (s = tp_vocab_embed(m, ids, M, h, stream)) != TP_OK) return s;
+  bool h_sq = false;  // the stage's input h comes without sums of squares
   for (int l = first; l < first + n; ++l)
-    if ((s = layer_forward(m, l, b, h, fused, ws, L, st)) != TP_OK) return s;
+    if ((s = layer_forward(m, l, b, h, fused, ws, L, st, &h_sq)) != TP_OK) return s;
   if (!logits) return TP_OK;
   uint16_t* hs = at<uint16_t>(ws, L.hs);
   TP_CHECK_CUDA(launch(m, "rmsnorm_final", st, [&] {

@@ -107,7 +107,7 @@ def test_ragged_prefill_matches_oracle():
     model.close()
 
 
-def _ragged_prefill(w, t, lens, seed):
+def _ragged_prefill(w, t, lens, seed, fused=True):
     model, _, _ = build_model(w, t, max_tokens=sum(lens))
     n = len(lens)
     ks = [model.alloc_kv(n, w.ctx)]
@@ -124,7 +124,7 @@ def _ragged_prefill(w, t, lens, seed):
     hx = synth.normal_f64(seed, 555, (M, w.hidden), 1.0)
     h = torch.from_numpy(hx.astype(np.float32)).to(torch.bfloat16).cuda()
     model.reset_stats()
-    model.layer_forward(0, batch, h)
+    model.layer_forward(0, batch, h, fused=fused)
     torch.cuda.synchronize()
     assert model.check_device() == 0
     launches = model.stats().kernel_launches
@@ -145,13 +145,16 @@ def test_short_prefill_with_norm_inside_the_gemms_matches_oracle(t):
     assert launches == 5  # qkv, attention, o_proj, gate_up, down_proj: no norm kernel
 
 
-def test_norm_kernels_return_above_32_tokens():
-    # 48 tokens: the RMSNorms run as kernels (unit weight; the norm weights are
-    # folded into qkv / gate_up either way)
+@pytest.mark.parametrize("fused", [True, False])
+def test_norm_paths_above_32_tokens(fused):
+    # 48 tokens: the first RMSNorm runs as a kernel (unit weight: its weight is
+    # folded into qkv); with the fused reduction o_proj leaves the sums of
+    # squares of h and gate_up applies the second norm itself, with the
+    # unfused one (per-rank partials + reduction kernel) it is a kernel too
     w = _wl("prefill", n_seqs=3, seq_len=16, ctx=16)
-    err, launches = _ragged_prefill(w, 2, [16, 16, 16], 7)
+    err, launches = _ragged_prefill(w, 2, [16, 16, 16], 7, fused=fused)
     assert err <= LAYER_TOL
-    assert launches == 7
+    assert launches == (6 if fused else 9)
 
 
 def test_sharded_equals_unsharded_on_gpu():
@@ -227,6 +230,37 @@ def test_two_layer_forward_with_padded_vocab_and_counters():
     ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
                     synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
     assert logits.shape == (w.n_seqs, w.vocab)
+    assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
+    model.close()
+
+
+@pytest.mark.parametrize("n_seqs,fused", [(6, True), (48, True), (48, False)])
+def test_three_layer_forward_norm_paths_match_oracle(n_seqs, fused):
+    # 6 tokens: every RMSNorm inside qkv / gate_up, from h's rows.  48
+    # tokens, fused: one norm kernel (layer 0's first), the rest inside the
+    # GEMMs from the sums of squares the fused row-parallel GEMMs leave.  48
+    # unfused: every norm a kernel.
+    w = _wl("decode", n_seqs=n_seqs, seq_len=1, ctx=40, vocab=1001, layers=3, embed=True)
+    t = 4
+    model, _, _ = build_model(w, t)
+    batch, _ = make_batch(model, w)
+    ids_np = synth.token_ids(w)
+    ids = torch.from_numpy(ids_np).cuda()
+    model.reset_stats()
+    logits = model.forward(ids, batch, fused=fused)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    per_layer = 5 if fused else 7  # qkv, attention, o_proj, gate_up, down (+2 reductions)
+    norms = 0 if n_seqs <= 32 else (1 if fused else 6)
+    assert model.stats().kernel_launches == 1 + 3 * per_layer + norms + 2  # embed ... head
+    dims = oracle_dims(w)
+    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
+    ob = oracle_batch(w)
+    for l in range(3):
+        kc, vc = oracle_caches(w, l, range(w.n_seqs))
+        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
+    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
+                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
 
