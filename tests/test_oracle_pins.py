@@ -82,6 +82,26 @@ def test_rmsnorm_closed_forms():
     assert np.allclose(np.mean(out * out, axis=-1), 1.0, rtol=1e-13)
 
 
+def test_rmsnorm_weight_folds_into_the_next_linear():
+    # the reading behind the CUDA path's decode layer: a norm's weight can be
+    # multiplied into the columns of the linear that reads its output, and the
+    # per-token 1/rms applied to that linear's output instead
+    H, N, M, eps = 96, 40, 5, 1e-5
+    w = 1.0 + rng.standard_normal(H) * 0.3
+    W = rng.standard_normal((N, H)) * 0.02
+    b = rng.standard_normal(N)
+    x = rng.standard_normal((M, H)) * 3
+    ref = O.linear(O.rmsnorm(x, w, eps), W, b)
+    rstd = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    folded = O.linear(x, W * w[None, :]) * rstd + b
+    assert np.allclose(folded, ref, rtol=1e-12, atol=1e-14)
+    # scaling the output rows by 1/rms of the wrong token, or folding w into
+    # the rows (output features) instead of the columns, is caught
+    assert not np.allclose(O.linear(x, W * w[None, :]) * rstd[::-1] + b, ref, rtol=1e-3)
+    Wr = W * w[:N, None]
+    assert not np.allclose(O.linear(x, Wr) * rstd + b, ref, rtol=1e-3)
+
+
 def test_silu_against_expit():
     x = np.linspace(-30, 30, 1001)
     assert np.allclose(O.silu(x), x * scipy.special.expit(x), rtol=1e-13, atol=1e-300)
