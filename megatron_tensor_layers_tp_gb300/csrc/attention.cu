@@ -183,21 +183,22 @@ struct DecSmem {
   // from the one it wants).
   static constexpr int kStages = D == 128 ? 4 : 8;
   static_assert(kStages % kDecGroups == 0, "stages must split evenly between the warp groups");
-  static constexpr int kComb = kDecWarps * 16 * (D + 2);  // floats: O, m, l per warp/row
+  // combine rows: O, m, l per warp/row; the pitch keeps the two rows a warp
+  // reads at once 18 banks apart (16 lanes per row, columns lane + 16 j)
+  static constexpr int kCombLd = D + 18;
+  static constexpr int kComb = kDecWarps * 16 * kCombLd;  // floats
   static constexpr size_t bytes(int) {
     return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
   }
 };
 
-// one output row slice of N fp32 values scaled by inv, stored as N bf16 (16 or 8 bytes)
+// N fp32 values of one output row scaled by inv, stored as bf16 at columns
+// dst[0], dst[16], dst[32], ... (a row's 16 threads write 32 contiguous bytes
+// per store)
 template <int N>
 __device__ __forceinline__ void store_out_row(uint16_t* dst, const float (&v)[N], float inv) {
-  static_assert(N == 8 || N == 4, "row slice of 8 or 4 columns");
-  uint32_t p[N / 2];
 #pragma unroll
-  for (int q = 0; q < N / 2; ++q) p[q] = pack2(v[2 * q] * inv, v[2 * q + 1] * inv);
-  if constexpr (N == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
-  else *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
+  for (int j = 0; j < N; ++j) dst[16 * j] = f_to_bf16(v[j] * inv);
 }
 
 template <int D>
@@ -342,40 +343,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
       }
       // combine: every warp's (m, l, O) meets the others in smem
-      float* cw = comb + warp * 16 * (D + 2);
+      constexpr int CL = L::kCombLd;
+      float* cw = comb + warp * 16 * CL;
       const int r0 = lane >> 2;
 #pragma unroll
       for (int nt = 0; nt < D / 8; ++nt) {
         const int col = nt * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(cw + r0 * (D + 2) + col) = make_float2(o[nt][0], o[nt][1]);
-        *reinterpret_cast<float2*>(cw + (r0 + 8) * (D + 2) + col) = make_float2(o[nt][2], o[nt][3]);
+        *reinterpret_cast<float2*>(cw + r0 * CL + col) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(cw + (r0 + 8) * CL + col) = make_float2(o[nt][2], o[nt][3]);
       }
       if ((lane & 3) == 0) {
-        cw[r0 * (D + 2) + D] = m[0]; cw[r0 * (D + 2) + D + 1] = l[0];
-        cw[(r0 + 8) * (D + 2) + D] = m[1]; cw[(r0 + 8) * (D + 2) + D + 1] = l[1];
+        cw[r0 * CL + D] = m[0]; cw[r0 * CL + D + 1] = l[0];
+        cw[(r0 + 8) * CL + D] = m[1]; cw[(r0 + 8) * CL + D + 1] = l[1];
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
-      // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128)
+      // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128): columns
+      // cl, cl + 16, ... so that a row's 16 threads read 16 consecutive floats
       constexpr int CPT = D / 16;
-      const int row = ctid >> 4, c0 = (ctid & 15) * CPT;
+      const int row = ctid >> 4, cl = ctid & 15;
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * (D + 2) + D]);
+      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * CL + D]);
       float ll = 0.f, acc[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
 #pragma unroll 2
       for (int w = 0; w < kDecWarps; ++w) {
-        const float* cr = comb + (w * 16 + row) * (D + 2);
+        const float* cr = comb + (w * 16 + row) * CL;
         const float mw = cr[D];
         if (mw == -INFINITY) continue;
         const float sc = exp2f(mw - mm);
         ll += cr[D + 1] * sc;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) acc[j] += cr[c0 + j] * sc;
+        for (int j = 0; j < CPT; ++j) acc[j] += cr[cl + 16 * j] * sc;
       }
       const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
-      uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + c0;
+      uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
       if (nseg == 1) {
         if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
       } else {
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         const int my_slot = (beg / TB == bg) ? 0 : 1;
         float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + c0 + j] = acc[j];
+        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + cl + 16 * j] = acc[j];
         if ((ctid & 15) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
         __threadfence();
         bar_sync(1, kDecWarps * 32);
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
             const float sc = exp2f(ms - M2);
             L2 += __ldcg(&src[row * (D + 2) + D + 1]) * sc;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + c0 + j]) * sc;
+            for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + cl + 16 * j]) * sc;
           }
           if (row < a.group) store_out_row<CPT>(orow, acc2, 1.f / L2);
           if (ctid == 0) a.tickets[bg] = 0;
