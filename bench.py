@@ -382,34 +382,43 @@ def run_ours(args, rank, world):
             "ms_per_step": round(ms_u / max(args.steps // 4, 20), 4),
             "extra_partial_bytes_per_row_op": 2 * args.t * w.tokens * w.hidden * 4}
 
-    # end to end through the public API: pinned host input -> device -> layer -> host
+    # end to end through the public API with host buffers: each step, the
+    # library's host-buffer call brings the pinned input rows to the device,
+    # runs the layer and writes the result rows back to pinned host memory
+    # (kernels reading/writing host memory over NVLink-C2C where the GPU is
+    # coherent with its host, volatile loads so every step fetches from host
+    # memory; cudaMemcpyAsync elsewhere)
     e2e_steps = max(min(args.steps, 500), 10)
     hin = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, pin_memory=True)
     hin.copy_(h.cpu())
     hout = torch.empty_like(hin, pin_memory=True)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            h.copy_(hin, non_blocking=True)
-            model.layer_forward(i % args.rotate, batch, h, bool(args.fused), stream=stream)
-            hout.copy_(h, non_blocking=True)
+            model.layer_forward_host(i % args.rotate, batch, hin, hout, h, bool(args.fused),
+                                     stream=stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     cb = batch.to_c()
+    model.reset_stats()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(e2e_steps):
-            h.copy_(hin, non_blocking=True)
-            model.layer_forward(i % args.rotate, batch, h, bool(args.fused), stream=stream, cbatch=cb)
-            hout.copy_(h, non_blocking=True)
+            model.layer_forward_host(i % args.rotate, batch, hin, hout, h, bool(args.fused),
+                                     stream=stream, cbatch=cb)
         e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    # two more kernels per step than the layer alone: the transfers ran as kernels
+    e2e_launches = model.stats().kernel_launches / e2e_steps
+    transfer = ("kernels reading/writing pinned host memory (NVLink-C2C)"
+                if round(e2e_launches) == round(launches / (args.steps + 0.0)) + 2
+                else "cudaMemcpyAsync")
     e2e = {"value": round(whole_job_rate(tokens, e2e_steps, ms_e2e, world), 1), "unit": UNIT,
            "h2d_bytes_per_step": w.tokens * w.hidden * 2, "d2h_bytes_per_step": w.tokens * w.hidden * 2,
-           "steps": e2e_steps}
+           "steps": e2e_steps, "call": "tp_layer_forward_host", "transfer": transfer}
 
     cpu = None
     if args.cpu_baseline and rank == 0 and world == 1:

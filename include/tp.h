@@ -268,6 +268,22 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
                            tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* tp_layer_forward on host-resident hidden rows (no counterpart on the
+ * pages; the call a host program makes when its hidden states live in host
+ * memory).  h_in_host [n_tokens, H] bf16 is brought to the caller's device
+ * buffer h_dev [n_tokens, H] (overwritten), the layer runs there, and the
+ * result is written to h_out_host [n_tokens, H].  Both host buffers must be
+ * pinned (cudaHostAlloc / cudaHostRegister; otherwise TP_ERR_ARG) and 16-byte
+ * aligned; they may be the same buffer, also across consecutive calls.  On a
+ * GPU that reaches host memory coherently (NVLink-C2C: GB300 with its Grace
+ * host) the two transfers are kernels that read and write the pinned memory
+ * directly and join the layer's chain of dependent launches; elsewhere they
+ * are cudaMemcpyAsync on `stream`.  Asynchronous: h_out_host is valid once
+ * `stream` has reached this point. */
+tp_status tp_layer_forward_host(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                                const tp_bf16* h_in_host, tp_bf16* h_out_host, tp_bf16* h_dev,
+                                int32_t fused, void* ws, size_t ws_bytes, void* stream);
+
 /* Full forward: vocab-parallel embedding of ids [n_tokens] into h, every
  * layer, final RMSNorm of the sampled rows, vocab-parallel LM head gathered
  * into logits [n_samples, vocab] (row stride ld_logits).

@@ -89,6 +89,8 @@ _SIGS = {
                                     c_size_t, c_void_p]),
     "tp_layer_forward": (c_int32, [c_void_p, c_int32, POINTER(tp_batch_t), c_void_p, c_int32,
                                    c_void_p, c_size_t, c_void_p]),
+    "tp_layer_forward_host": (c_int32, [c_void_p, c_int32, POINTER(tp_batch_t), c_void_p, c_void_p,
+                                        c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "tp_forward": (c_int32, [c_void_p, c_void_p, POINTER(tp_batch_t), c_void_p, c_void_p, c_int64,
                              c_int32, c_void_p, c_size_t, c_void_p]),
     "tp_stage_forward": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, POINTER(tp_batch_t),
@@ -207,6 +209,12 @@ def tp_lm_head_gather(model, x, S, logits, ld_logits, ws, ws_bytes, stream) -> i
 
 def tp_layer_forward(model, layer, batch: tp_batch_t, h, fused, ws, ws_bytes, stream) -> int:
     return lib().tp_layer_forward(model, layer, ctypes.byref(batch), h, fused, ws, ws_bytes, stream)
+
+
+def tp_layer_forward_host(model, layer, batch: tp_batch_t, h_in_host, h_out_host, h_dev, fused, ws,
+                          ws_bytes, stream) -> int:
+    return lib().tp_layer_forward_host(model, layer, ctypes.byref(batch), h_in_host, h_out_host,
+                                       h_dev, fused, ws, ws_bytes, stream)
 
 
 def tp_forward(model, ids, batch: tp_batch_t, h, logits, ld_logits, fused, ws, ws_bytes,

@@ -315,6 +315,46 @@ cudaError_t launch_fold_cols(uint16_t* dst, const uint16_t* src, const uint16_t*
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Host <-> device transfers of the host-buffer entry point, as kernels: on a
+// GPU that reaches host memory coherently (NVLink-C2C) a kernel can read and
+// write pinned host memory directly, so the step's chain of programmatically
+// dependent launches is not broken by copy-engine operations.  Both wait for
+// their predecessor before touching memory (the host buffers may be reused
+// from one call to the next).  Host loads are volatile (ld.cv: fetched from
+// host memory every time, never from a cached line) and host stores write
+// through.  16-byte vectors, grid-stride.
+// ---------------------------------------------------------------------------
+__global__ void host_in_kernel(const uint4* __restrict__ src_host, uint4* __restrict__ dst,
+                               int64_t n16) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += stride)
+    dst[i] = __ldcv(src_host + i);
+}
+
+__global__ void host_out_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst_host,
+                                int64_t n16) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += stride)
+    __stwt(dst_host + i, src[i]);
+}
+
+cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, bool to_host,
+                             cudaStream_t st) {
+  const int64_t n16 = (int64_t)(bytes / 16);
+  if (n16 == 0) return cudaSuccess;
+  const int blocks = (int)std::min<int64_t>((n16 + 255) / 256, 1024);
+  if (to_host)
+    return launch_k(host_out_kernel, dim3(blocks), dim3(256), 0, st,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return launch_k(host_in_kernel, dim3(blocks), dim3(256), 0, st, static_cast<const uint4*>(src),
+                  static_cast<uint4*>(dst), n16);
+}
+
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;

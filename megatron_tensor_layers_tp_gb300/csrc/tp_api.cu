@@ -39,6 +39,7 @@ struct tp_model {
   tp_config_t cfg;
   int device = 0;
   int num_sms = 0;
+  bool host_coherent = false;  // the GPU reaches host memory coherently (NVLink-C2C)
   std::vector<LayerShards> layers;
   uint16_t* embed = nullptr;  // [Vp][H] = t shards of [Vp/t][H]
   ShardedLinear lm;
@@ -635,6 +636,11 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
   if (cudaGetDevice(&m->device) != cudaSuccess) return fail(TP_ERR_CUDA);
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return fail(TP_ERR_CUDA);
+  {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrHostNativeAtomicSupported, m->device) == cudaSuccess)
+      m->host_coherent = v != 0;
+  }
   // the attention block is sharded over the attn_tp ranks of a DP group, the
   // MLP over all t ranks
   const int t = cfg.t, at = cfg.attn_tp, H = cfg.hidden, d = cfg.head_dim;
@@ -1049,6 +1055,48 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
   bool h_sq = false;  // the caller's h comes without sums of squares
   return layer_forward(m, layer, b, h_inout, fused, ws, ws_layout(m, b->n_tokens),
                        static_cast<cudaStream_t>(stream), &h_sq);
+}
+
+// The device address of pinned (page-locked) host memory, or false for any
+// other pointer.
+static bool pinned_device_ptr(const void* p, void** out) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return false;
+  *out = at.devicePointer;
+  return true;
+}
+
+tp_status tp_layer_forward_host(const tp_model* m, int32_t layer, const tp_batch_t* b,
+                                const tp_bf16* h_in_host, tp_bf16* h_out_host, tp_bf16* h_dev,
+                                int32_t fused, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_layer(m, layer) || !h_in_host || !h_out_host || !h_dev || !aligned16(h_dev) ||
+      !aligned16(h_in_host) || !aligned16(h_out_host))
+    return TP_ERR_ARG;
+  tp_status s = check_batch(m, b);
+  if (s != TP_OK) return s;
+  if (!ws_ok(m, b->n_tokens, ws, ws_bytes)) return TP_ERR_WORKSPACE;
+  void *din = nullptr, *dout = nullptr;
+  if (!pinned_device_ptr(h_in_host, &din) || !pinned_device_ptr(h_out_host, &dout))
+    return TP_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)b->n_tokens * m->cfg.hidden * 2;  // H % 64 == 0: a multiple of 16
+  if (m->host_coherent) {
+    TP_CHECK_CUDA(launch(m, "host_in", st, [&] { return launch_host_copy(din, h_dev, bytes, false, st); }));
+  } else {
+    TP_CHECK_CUDA(cudaMemcpyAsync(h_dev, h_in_host, bytes, cudaMemcpyHostToDevice, st));
+  }
+  bool h_sq = false;
+  if ((s = layer_forward(m, layer, b, h_dev, fused, ws, ws_layout(m, b->n_tokens), st, &h_sq)) !=
+      TP_OK)
+    return s;
+  if (m->host_coherent)
+    return cuda_status(
+        launch(m, "host_out", st, [&] { return launch_host_copy(h_dev, dout, bytes, true, st); }));
+  return cuda_status(cudaMemcpyAsync(h_out_host, h_dev, bytes, cudaMemcpyDeviceToHost, st));
 }
 
 // Layers [first, first + n) on h; the embedding first when ids is set, the

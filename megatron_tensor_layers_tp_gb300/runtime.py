@@ -193,6 +193,17 @@ class TPModel:
                                    _stream(stream)), "tp_layer_forward")
         return h
 
+    def layer_forward_host(self, layer: int, batch: Batch, h_in_host: torch.Tensor,
+                           h_out_host: torch.Tensor, h_dev: torch.Tensor, fused: bool = True,
+                           stream=None, cbatch: Optional[B.tp_batch_t] = None) -> torch.Tensor:
+        """tp_layer_forward_host: pinned host rows in, the layer on h_dev, host rows out."""
+        self.ensure_workspace(batch.n_tokens, stream)
+        cb = cbatch if cbatch is not None else batch.to_c()
+        B.check(B.tp_layer_forward_host(self.handle, layer, cb, h_in_host.data_ptr(),
+                                        h_out_host.data_ptr(), h_dev.data_ptr(), int(fused),
+                                        *self.ws_args, _stream(stream)), "tp_layer_forward_host")
+        return h_out_host
+
     def forward(self, ids: torch.Tensor, batch: Batch, fused: bool = True, stream=None,
                 h: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                 cbatch: Optional[B.tp_batch_t] = None):

@@ -79,6 +79,8 @@ def test_calls_without_a_model_are_rejected_on_the_host():
     assert B.tp_vocab_embed(None, 0, 4, 0, 0) == ST["TP_ERR_ARG"]
     assert B.tp_lm_head_gather(None, 0, 1, 0, 0, 0, 0, 0) == ST["TP_ERR_ARG"]
     assert B.tp_rmsnorm(None, 0, 0, 1, 0, 0) == ST["TP_ERR_ARG"]
+    assert B.lib().tp_layer_forward_host(None, 0, None, None, None, None, 1, None, 0, None) == \
+        ST["TP_ERR_ARG"]
     assert B.lib().tp_get_stats(None, None) == ST["TP_ERR_ARG"]
     for code, name in B.STATUS_NAMES.items():
         assert B.strerror(code) and B.strerror(code) != "unknown status", name
