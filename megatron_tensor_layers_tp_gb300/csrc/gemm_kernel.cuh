@@ -4,17 +4,28 @@
 //
 // One launch covers all t emulated ranks.  Operands are 3-D tensor maps
 // (K, rows, slice) where the slice coordinate is the rank shard.  Work is the
-// flat sequence of (output tile, 64-wide K step) pairs; CTA c of G processes
-// the contiguous range [c*T/G, (c+1)*T/G) ("stream-K"), so every CTA streams
-// the same number of bytes.  A tile cut between CTAs leaves fp32 partials in
-// the workspace; the last CTA to finish a piece of the tile (atomic ticket, no
-// waiting) adds the pieces in K order — which is rank order for the fused
-// row-parallel reduction — and runs the epilogue.  The result is deterministic
-// for a given grid.
+// flat sequence of (output tile, 64-wide K step) pairs, scheduled (on the
+// host) one of three ways:
+//  - stream-K: CTA c of G processes the contiguous range [c*T/G, (c+1)*T/G),
+//    so every CTA streams the same number of bytes.  A tile cut between CTAs
+//    leaves fp32 partials in the workspace; the last CTA to finish a piece of
+//    the tile (atomic ticket, no waiting) adds the pieces in K order — which
+//    is rank order for the fused row-parallel reduction — and runs the
+//    epilogue;
+//  - cluster split-K (decode orientation, few tiles): a cluster of s CTAs per
+//    tile, each taking 1/s of its K range; the pieces meet in distributed
+//    shared memory and are added in K order after a cluster barrier;
+//  - data-parallel waves of whole tiles (prefill orientation), the remainder
+//    as a last, partial wave of whole tiles.
+// The result is deterministic for a given grid.
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 issues tcgen05.mma from
-// one thread into one of two TMEM accumulators, warps 2..5 drain the other
-// accumulator (tcgen05.ld) and run the epilogue.  Every wait is bounded.
+// Roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma from one thread
+// into one of two TMEM accumulators, and the epilogue warps (eight in the
+// decode orientation, 320 threads; four in the prefill orientation, 192)
+// drain the other accumulator (tcgen05.ld) and run the epilogue.  In the
+// decode orientation the qkv and gate_up epilogue warps also work out each
+// token's 1/rms for the RMSNorm folded into those GEMMs while the weights
+// stream.  Every wait is bounded.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -532,9 +543,9 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
   };
 
   // Epilogue inputs of this CTA's last segment: that segment's epilogue (or
-  // fix-up) ends the kernel, so in the decode orientation (one 16-column
-  // chunk) its global inputs are fetched as soon as the epilogue warps may
-  // read them, long before the accumulator is ready.
+  // fix-up) ends the kernel, so in the decode orientation (few 8-column units
+  // per thread) the inputs of its first unit are fetched as soon as the
+  // epilogue warps may read them, long before the accumulator is ready.
   EpiIn pre;
   bool pre_ok = false;
   int n_segs = 0;
