@@ -12,9 +12,11 @@
 // K/V tiles of 64 positions arrive by TMA (128-byte swizzle) and feed
 // mma.sync tiles from ldmatrix; scores and the online softmax stay in fp32.
 //   decode : one query token per sequence; the (sequence, KV head, key tile)
-//            space is split evenly over a persistent grid ("stream-K"); pieces
-//            of one (sequence, KV head) are combined in key order by the last
-//            CTA to finish one (atomic ticket, no waiting).
+//            space is split evenly over the grid: whole (sequence, KV head)
+//            pairs per CTA when the host finds such a grid that fills the
+//            GPU with short enough streams, otherwise a flat split over all
+//            SMs whose pieces of one pair are combined in key order by the
+//            last CTA to finish one (atomic ticket, no waiting).
 //   prefill: causal; one CTA per (sequence, Q head, 64-token query block).
 #include <cuda.h>
 #include <cuda_bf16.h>
