@@ -146,7 +146,7 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
-        except Exception:
+        except OSError:  # no nvidia-smi on this machine: no clock samples
             self.proc = None
 
     def _read(self):
@@ -160,7 +160,7 @@ class ClockSampler:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
-            except Exception:
+            except subprocess.TimeoutExpired:
                 self.proc.kill()
 
     def summary(self, t0, t1):
