@@ -26,18 +26,19 @@ def _hidden(w):
 
 
 @pytest.mark.parametrize("mode,n_seqs,seq_len,ctx", [("decode", 16, 1, 300), ("decode", 48, 1, 90),
-                                                     ("prefill", 3, 40, 40)])
-def test_host_entry_point_equals_device_layer(mode, n_seqs, seq_len, ctx):
+                                                     ("prefill", 4, 30, 30)])
+@pytest.mark.parametrize("fused,attn_dp", [(True, 1), (False, 1), (True, 2)])
+def test_host_entry_point_equals_device_layer(mode, n_seqs, seq_len, ctx, fused, attn_dp):
     w = _wl(mode, n_seqs, seq_len, ctx)
-    model, _, _ = build_model(w, 4)
+    model, _, _ = build_model(w, 4, attn_dp=attn_dp)
     batch, _ = make_batch(model, w)
     h0 = _hidden(w)
     ref = h0.clone()
-    model.layer_forward(0, batch, ref)
+    model.layer_forward(0, batch, ref, fused=fused)
     hin = h0.cpu().pin_memory()
     hout = torch.zeros_like(hin).pin_memory()
     hdev = torch.empty_like(h0)
-    model.layer_forward_host(0, batch, hin, hout, hdev)
+    model.layer_forward_host(0, batch, hin, hout, hdev, fused=fused)
     torch.cuda.synchronize()
     assert model.check_device() == 0
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
