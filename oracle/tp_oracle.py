@@ -312,6 +312,23 @@ def lm_head(h_rows: Array, final_norm: Array, W_lm: Array, dims: Dims,
     return rb(linear(x, W_lm))
 
 
+def forward(ids: Array, E: Array, layers, final_norm: Array, W_lm: Array, batch: Batch,
+            dims: Dims, rb: Callable = round_bf16, rows: Optional[Array] = None) -> Array:
+    """The whole decoder forward in the order the pages draw it
+    ("张量、流水线与数据并行", §线性层怎么切 flowchart and §输出层): the embedding
+    lookup, then every layer in turn (attention block, then MLP), then the
+    final RMSNorm and the LM head on the sampled rows.
+
+    layers: iterable of (LayerWeights, kcache, vcache) in layer order (a
+    generator may build each layer's weights on demand); rows: the token rows
+    whose logits are returned (default: the last token of each sequence)."""
+    h = embed(E, ids)
+    for W, kc, vc in layers:
+        h = layer_forward(h, W, kc, vc, batch, dims, rb)
+    sel = batch.sample_rows() if rows is None else np.asarray(rows)
+    return lm_head(h[sel], final_norm, W_lm, dims, rb)
+
+
 # ---------------------------------------------------------------------------
 # sharded emulation (t ranks, in order 0..t-1)
 # ---------------------------------------------------------------------------

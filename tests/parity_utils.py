@@ -129,6 +129,31 @@ def make_batch(model, w: Workload, caches=None):
     return prefill_batch(w.n_seqs, w.seq_len, ks, vs, w.l_max), caches
 
 
+def oracle_forward(w: Workload, ids_np, seqs: Sequence[int] = None):
+    """The oracle's logits for workload w (embedding, every layer, final norm,
+    LM head at each sequence's last token); ``seqs`` restricts a decode
+    workload to those sequences (independent of the others), weights and
+    caches regenerated layer by layer."""
+    import oracle as O
+    dims = oracle_dims(w)
+    if seqs is None:
+        seqs = list(range(w.n_seqs))
+        ob = oracle_batch(w)
+        ids_sel = ids_np
+    else:
+        assert w.mode == "decode"
+        ob = O.Batch.decode(len(seqs), w.ctx)
+        ids_sel = np.asarray(ids_np)[list(seqs)]
+
+    def layers():
+        for l in range(w.n_layers):
+            kc, vc = oracle_caches(w, l, seqs)
+            yield oracle_layer(w, l), kc, vc
+    return O.forward(ids_sel, synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), layers(),
+                     synth.host_weight(w, "final_norm", 0, (w.hidden,)),
+                     synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), ob, dims)
+
+
 def oracle_batch(w: Workload):
     import oracle as O
     if w.mode == "decode":
@@ -152,16 +177,7 @@ def run_tiny_forward_check(t: int = 2, tol: float = 5e-2) -> float:
     st = model.check_device()
     assert st == 0, f"device status {st}"
     gpu = to_f64(logits)
-    # oracle
-    dims = oracle_dims(w)
-    E = synth.host_weight(w, "embed", 0, (w.vocab, w.hidden))
-    h = O.embed(E, ids_np)
-    kc, vc = oracle_caches(w, 0, range(w.n_seqs))
-    ob = oracle_batch(w)
-    h = O.layer_forward(h, oracle_layer(w, 0), kc, vc, ob, dims)
-    rows = ob.sample_rows()
-    ref = O.lm_head(h[rows], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    ref = oracle_forward(w, ids_np)
     err = rel_err(gpu, ref)
     model.close()
     if not err <= tol:

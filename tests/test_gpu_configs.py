@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 import oracle as O  # noqa: E402
 import synth  # noqa: E402
 from tests.parity_utils import (build_model, make_batch, oracle_batch, oracle_caches,  # noqa: E402
-                                oracle_dims, oracle_layer, rel_err, run_tiny_forward_check, to_f64)
+                                oracle_dims, oracle_forward, oracle_layer, rel_err,
+                                run_tiny_forward_check, to_f64)
 
 LAYER_TOL = 2e-2
 LOGIT_TOL = 5e-2
@@ -80,13 +81,7 @@ def test_config_llama8b_prefill_with_embed_and_head():
     gpu = to_f64(logits)
     model.close()
     torch.cuda.empty_cache()
-    dims = oracle_dims(w)
-    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
-    kc, vc = oracle_caches(w, 0, range(w.n_seqs))
-    ob = oracle_batch(w)
-    h = O.layer_forward(h, oracle_layer(w, 0), kc, vc, ob, dims)
-    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    ref = oracle_forward(w, ids_np)
     assert gpu.shape == (8, w.vocab)
     assert rel_err(gpu, ref) <= LOGIT_TOL
 
@@ -109,13 +104,9 @@ def test_config_llama8b_full_32_layers_sampled_sequences():
     model.close()
     del batch
     torch.cuda.empty_cache()
-    sample = [0, 37]
-    dims = oracle_dims(w)
-    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np[sample])
-    ob = O.Batch.decode(len(sample), w.ctx)
-    for l in range(w.n_layers):
-        kc, vc = oracle_caches(w, l, sample)
-        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
-    ref = O.lm_head(h, synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
-    assert rel_err(gpu[sample], ref) <= LOGIT_TOL
+    # decode sequences are independent: the oracle takes 8 of the 64, spread
+    # over the batch (first and last included), through all 32 layers
+    sample = [0, 9, 18, 27, 37, 46, 55, 63]
+    ref = oracle_forward(w, ids_np, seqs=sample)
+    for i, b in enumerate(sample):
+        assert rel_err(gpu[b], ref[i]) <= LOGIT_TOL, b

@@ -2,6 +2,8 @@
 sizes the oracle finishes in seconds (several tiles, ragged tails, KV
 replication), plus GPU-side invariants: sharded vs unsharded (t vs t=1),
 decode step vs prefill row, determinism and the collective counters."""
+from dataclasses import replace
+
 import numpy as np
 import pytest
 
@@ -13,7 +15,7 @@ import synth  # noqa: E402
 from megatron_tensor_layers_tp_gb300 import binding as B  # noqa: E402
 from megatron_tensor_layers_tp_gb300.runtime import Batch  # noqa: E402
 from tests.parity_utils import (build_model, make_batch, oracle_batch, oracle_caches,  # noqa: E402
-                                oracle_dims, oracle_layer, rel_err, to_f64)
+                                oracle_dims, oracle_forward, oracle_layer, rel_err, to_f64)
 
 LAYER_TOL = 2e-2
 LOGIT_TOL = 5e-2
@@ -221,14 +223,7 @@ def test_two_layer_forward_with_padded_vocab_and_counters():
     assert st.allreduce_payload_bytes == (2 * 2 + 1) * w.tokens * w.hidden * 2
     assert st.allgathers == 1
     assert st.allgather_recv_bytes_per_rank == w.n_seqs * ((t - 1) * w.vocab * 2 // t)
-    dims = oracle_dims(w)
-    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
-    ob = oracle_batch(w)
-    for l in range(2):
-        kc, vc = oracle_caches(w, l, range(w.n_seqs))
-        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
-    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    ref = oracle_forward(w, ids_np)
     assert logits.shape == (w.n_seqs, w.vocab)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
@@ -253,14 +248,7 @@ def test_three_layer_forward_norm_paths_match_oracle(n_seqs, fused):
     per_layer = 5 if fused else 7  # qkv, attention, o_proj, gate_up, down (+2 reductions)
     norms = 0 if n_seqs <= 32 else (1 if fused else 6)
     assert model.stats().kernel_launches == 1 + 3 * per_layer + norms + 2  # embed ... head
-    dims = oracle_dims(w)
-    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
-    ob = oracle_batch(w)
-    for l in range(3):
-        kc, vc = oracle_caches(w, l, range(w.n_seqs))
-        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
-    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    ref = oracle_forward(w, ids_np)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
 
@@ -279,3 +267,35 @@ def test_decode_layer_4096_wide_ragged_tokens_matches_oracle(n_seqs):
     model2, h2, _ = _run_layer(w, 8, fused=False)
     assert rel_err(to_f64(h2), to_f64(h)) <= 1e-2
     model.close(); model2.close()
+
+
+@pytest.mark.parametrize("t", [1, 8])
+@pytest.mark.parametrize("ctx", [1, 2, 65, 129])
+def test_decode_context_edges_match_oracle(t, ctx):
+    # ctx 1: the new token is the whole context (its attention output is its
+    # own v); ctx 2: one cached key; ctx 65 / 129: the last 64-key tile holds
+    # a single key
+    w = _wl("decode", n_seqs=5, seq_len=1, ctx=ctx, n_kv=8)
+    model, h, (ks, vs) = _run_layer(w, t)
+    ref, kc, vc = _oracle_layer(w)
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    gv = _cache_logical(model, vs[0], w)
+    for b in range(w.n_seqs):
+        assert rel_err(gv[b][:, ctx - 1], vc[b][:, ctx - 1]) <= LAYER_TOL
+    model.close()
+
+
+@pytest.mark.parametrize("n_seqs", [6, 64])
+def test_attention_with_dominant_scores_matches_oracle(n_seqs):
+    # cached keys and values ~N(0, 60^2): the scores q.k / sqrt(d) spread over
+    # tens of units, so each softmax is close to one-hot and a slip in the
+    # running maximum or the rescaling of the online softmax shows up at once;
+    # the attention output (values of size ~60) dominates the layer's output.
+    # 6 sequences: each (sequence, KV head) pair's key tiles are split over
+    # several CTAs and combined; 64: whole pairs per CTA
+    w = replace(_wl("decode", n_seqs=n_seqs, seq_len=1, ctx=300, n_kv=2), sigma_kv=60.0)
+    for t in (1, 4):
+        model, h, _ = _run_layer(w, t)
+        ref, _, _ = _oracle_layer(w)
+        assert rel_err(to_f64(h), ref) <= LAYER_TOL, t
+        model.close()

@@ -4,9 +4,9 @@ next) and CUDA-graph capture of a decode step (the fixed per-step cost that
 CUDA graph addresses, "Tensor Parallelism 执行路径", 每 token 的通信量).
 
 Both only re-package the same kernels, so they are checked bit for bit
-against the eager tp_forward / tp_layer_forward, and the eager forward is
-itself checked against the oracle in test_gpu_layer.py; one case here also
-checks the staged logits against the oracle directly."""
+against the eager tp_forward / tp_layer_forward, and also directly against
+the oracle: the staged logits, the replayed forward's logits (twice, with
+different token ids) and the replayed decode layer."""
 import numpy as np
 import pytest
 
@@ -17,9 +17,10 @@ import oracle as O  # noqa: E402
 import synth  # noqa: E402
 from megatron_tensor_layers_tp_gb300 import binding as B  # noqa: E402
 from tests.parity_utils import (build_model, make_batch, oracle_batch, oracle_caches,  # noqa: E402
-                                oracle_dims, oracle_layer, rel_err, to_f64)
+                                oracle_dims, oracle_forward, oracle_layer, rel_err, to_f64)
 
 LOGIT_TOL = 5e-2
+LAYER_TOL = 2e-2
 
 
 def _wl(n_seqs=6, ctx=40, layers=4, hidden=256, n_heads=4, n_kv=2, head_dim=64, inter=768,
@@ -91,14 +92,7 @@ def test_staged_logits_match_oracle():
     model.stage_forward(1, 1, batch, b, logits=logits)
     torch.cuda.synchronize()
     assert model.check_device() == 0
-    dims = oracle_dims(w)
-    h = O.embed(synth.host_weight(w, "embed", 0, (w.vocab, w.hidden)), ids_np)
-    ob = oracle_batch(w)
-    for l in range(2):
-        kc, vc = oracle_caches(w, l, range(w.n_seqs))
-        h = O.layer_forward(h, oracle_layer(w, l), kc, vc, ob, dims)
-    ref = O.lm_head(h[ob.sample_rows()], synth.host_weight(w, "final_norm", 0, (w.hidden,)),
-                    synth.host_weight(w, "lm_head", 0, (w.vocab, w.hidden)), dims)
+    ref = oracle_forward(w, ids_np)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
 
@@ -145,6 +139,8 @@ def test_graph_forward_replays_eager(t):
     assert model.check_device() == 0
     assert torch.equal(_bits(logits), _bits(logits_ref))
     assert torch.equal(_bits(h), _bits(h_ref))
+    # and the replay against the oracle itself
+    assert rel_err(to_f64(logits), oracle_forward(w, ids_np)) <= LOGIT_TOL
     st = model.stats()
     assert st.allreduces == 2 * w.n_layers + 1 and st.allgathers == 1
     assert st.kernel_launches > 0
@@ -156,6 +152,7 @@ def test_graph_forward_replays_eager(t):
     _, logits_ref2 = _eager(model, w, batch, ids)
     assert torch.equal(_bits(logits), _bits(logits_ref2))
     assert not torch.equal(_bits(logits_ref2), _bits(logits_ref))
+    assert rel_err(to_f64(logits), oracle_forward(w, ids2_np)) <= LOGIT_TOL
     graph.close()
     model.close()
 
@@ -178,6 +175,11 @@ def test_graph_layer_replays_eager_at_decode_shape():
     stream.synchronize()
     assert model.check_device() == 0
     assert torch.equal(_bits(h), _bits(ref))
+    # the replayed layer against the oracle
+    kc, vc = oracle_caches(w, 0, range(w.n_seqs))
+    want = O.layer_forward(synth.host_hidden(w), oracle_layer(w, 0), kc, vc, oracle_batch(w),
+                           oracle_dims(w))
+    assert rel_err(to_f64(h), want) <= LAYER_TOL
     # replay twice more from the same input: identical
     for _ in range(2):
         with torch.cuda.stream(stream):
