@@ -93,6 +93,11 @@ typedef struct {
   float rope_theta;      /* RoPE base */
   int32_t max_positions; /* RoPE table length: every position must be < this */
   int32_t attn_dp;       /* attention data-parallel groups (0 or 1: none) */
+  int32_t host_io;       /* tp_layer_forward_host transfers: 0 = chosen from the
+                            device (kernels over a coherent host link, else the
+                            copy engine), 1 = always cudaMemcpyAsync */
+  int32_t plain_column_shards; /* 1: keep an unfolded copy of every qkv / gate_up
+                            shard for tp_column_linear (see tp_load_shards) */
   /* derived, written by tp_config */
   int32_t vocab_padded;
   int32_t vocab_per_rank;
@@ -145,14 +150,22 @@ typedef struct tp_model tp_model; /* opaque: owns the shard buffers */
  * Within a shard, rows are stored in the order the fused epilogues want (the
  * two halves of each RoPE pair, and each gate row with its up row, sit next
  * to each other); every output of the API is in the standard order.
- * The decoder layer path also keeps a second copy of every qkv and gate_up
- * shard with the preceding RMSNorm's weight folded into its columns
- * (W[n][k] * w[k], rounded to bf16): (x / rms(x) * w) . W[n] equals
- * (x . (W[n] * w)) / rms(x).  tp_column_linear uses the plain shards. */
+ * The decoder layer reads qkv and gate_up shards with the preceding RMSNorm's
+ * weight folded into their columns (W[n][k] * w[k], rounded to bf16):
+ * (x / rms(x) * w) . W[n] equals (x . (W[n] * w)) / rms(x).  tp_column_linear
+ * computes with the unfolded weights.  When a layer's norm weight is exactly
+ * 1 everywhere the folded and unfolded shards are the same bytes and one
+ * buffer serves both; otherwise the unfolded copy (2 bytes per qkv and
+ * gate_up weight, 285 MB per Llama-3.1-8B layer) is kept only when
+ * cfg->plain_column_shards = 1, and tp_column_linear on a layer without it
+ * returns TP_ERR_UNSUPPORTED. */
 tp_status tp_load_shards(const tp_config_t* cfg, const tp_weights_t* w, void* stream,
                          tp_model** out);
 void tp_free(tp_model* m);
 tp_status tp_get_config(const tp_model* m, tp_config_t* out);
+/* Device memory the model owns (every shard, the RoPE table, the status
+ * word), in bytes, in *bytes. */
+tp_status tp_model_bytes(const tp_model* m, int64_t* bytes);
 
 /* Workspace bytes needed by any call on up to max_tokens rows. */
 size_t tp_workspace_bytes(const tp_model* m, int32_t max_tokens);
@@ -173,7 +186,9 @@ enum { TP_QKV = 0, TP_GATE_UP = 1, TP_O = 2, TP_DOWN = 3 };
  *           N_r = 2 I/t for TP_GATE_UP (gate slice, then up slice).
  *           y_rank_stride >= M*N_r.
  * Plain GEMM output plus the rank's slice of the layer's bias when the model
- * has one (bq/bk/bv or bg/bu): no RoPE, no activation. */
+ * has one (bq/bk/bv or bg/bu): no RoPE, no activation.  TP_ERR_UNSUPPORTED
+ * when the model keeps no unfolded copy of this layer's shards (see
+ * tp_load_shards). */
 tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
                            int32_t M, tp_bf16* y, int64_t y_rank_stride, void* ws,
                            size_t ws_bytes, void* stream);
@@ -277,9 +292,12 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
  * aligned; they may be the same buffer, also across consecutive calls.  On a
  * GPU that reaches host memory coherently (NVLink-C2C: GB300 with its Grace
  * host) the two transfers are kernels that read and write the pinned memory
- * directly and join the layer's chain of dependent launches; elsewhere they
- * are cudaMemcpyAsync on `stream`.  Asynchronous: h_out_host is valid once
- * `stream` has reached this point. */
+ * directly and join the layer's chain of dependent launches; elsewhere, or
+ * when the model was configured with host_io = 1, they are cudaMemcpyAsync on
+ * `stream`.  The GPU counts as coherent with its host when it reports both
+ * native atomics over the host link and access to pageable host memory
+ * through the host's page tables (true of NVLink-C2C, false of PCIe).
+ * Asynchronous: h_out_host is valid once `stream` has reached this point. */
 tp_status tp_layer_forward_host(const tp_model* m, int32_t layer, const tp_batch_t* b,
                                 const tp_bf16* h_in_host, tp_bf16* h_out_host, tp_bf16* h_dev,
                                 int32_t fused, void* ws, size_t ws_bytes, void* stream);
@@ -368,8 +386,10 @@ void tp_graph_free(tp_graph* g);
  *     requests return TP_ERR_WORKSPACE.  The tickets are cleared on `stream`
  *     before each launch.
  *   Set-up: the first call on each device resolves the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     life of the process; make that first call before any stream capture,
+ *     and do not call the entry point on a device after cudaDeviceReset
+ *     (the address belonged to the destroyed context).
  *   Concurrency: every call shares the one array, so calls that may overlap
  *     on the GPU (different streams, or different host threads) race; order
  *     them on one stream.
@@ -379,6 +399,12 @@ tp_status tp_row_linear_reduce_noalloc(const tp_model* m, int32_t layer, int32_t
                                        const tp_bf16* x, int64_t x_rank_stride, int64_t ldx,
                                        int32_t M, const tp_bf16* residual, tp_bf16* y,
                                        void* stream);
+
+/* Whether tp_row_linear_reduce_noalloc's fixed scratch can hold a call of M
+ * tokens with `hidden` output features on a GPU with num_sms SMs (1) or the
+ * call would return TP_ERR_WORKSPACE (0).  Pure host arithmetic: no CUDA
+ * call, usable without a GPU. */
+int32_t tp_row_linear_reduce_noalloc_fits(int32_t M, int32_t hidden, int32_t num_sms);
 
 /* Replicated RMSNorm (P1 §3.2: small layers stay whole on every rank):
  * y = x / sqrt(mean(x^2) + eps) * w, fp32 arithmetic, bf16 in and out.

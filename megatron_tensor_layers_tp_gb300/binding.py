@@ -27,7 +27,7 @@ class tp_config_t(Structure):
     _fields_ = [(n, c_int32) for n in ("hidden", "n_heads", "n_kv_heads", "head_dim", "intermediate",
                                        "vocab", "n_layers", "t")] + \
                [("rms_eps", c_float), ("rope_theta", c_float), ("max_positions", c_int32),
-                ("attn_dp", c_int32)] + \
+                ("attn_dp", c_int32), ("host_io", c_int32), ("plain_column_shards", c_int32)] + \
                [(n, c_int32) for n in ("vocab_padded", "vocab_per_rank", "q_heads_per_rank",
                                        "kv_heads_per_rank", "kv_replicas", "kv_copies",
                                        "inter_per_rank", "attn_tp")]
@@ -77,6 +77,7 @@ _SIGS = {
                                  POINTER(c_void_p)]),
     "tp_free": (None, [c_void_p]),
     "tp_get_config": (c_int32, [c_void_p, POINTER(tp_config_t)]),
+    "tp_model_bytes": (c_int32, [c_void_p, POINTER(c_int64)]),
     "tp_workspace_bytes": (c_size_t, [c_void_p, c_int32]),
     "tp_workspace_init": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "tp_column_linear": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int64,
@@ -106,6 +107,7 @@ _SIGS = {
     "tp_graph_free": (None, [c_void_p]),
     "tp_row_linear_reduce_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_int64,
                                                c_int64, c_int32, c_void_p, c_void_p, c_void_p]),
+    "tp_row_linear_reduce_noalloc_fits": (c_int32, [c_int32, c_int32, c_int32]),
     "tp_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "tp_get_stats": (c_int32, [c_void_p, POINTER(tp_stats_t)]),
     "tp_reset_stats": (None, [c_void_p]),
@@ -175,6 +177,12 @@ def tp_get_config(model: int) -> tp_config_t:
     return c
 
 
+def tp_model_bytes(model: int) -> int:
+    v = c_int64(0)
+    check(lib().tp_model_bytes(model, ctypes.byref(v)), "tp_model_bytes")
+    return v.value
+
+
 def tp_workspace_bytes(model: int, max_tokens: int) -> int:
     return lib().tp_workspace_bytes(model, max_tokens)
 
@@ -197,6 +205,10 @@ def tp_row_linear_reduce_noalloc(model, layer, which, x, x_rank_stride, ldx, M, 
                                  stream) -> int:
     return lib().tp_row_linear_reduce_noalloc(model, layer, which, x, x_rank_stride, ldx, M,
                                               residual, y, stream)
+
+
+def tp_row_linear_reduce_noalloc_fits(M, hidden, num_sms) -> int:
+    return lib().tp_row_linear_reduce_noalloc_fits(M, hidden, num_sms)
 
 
 def tp_vocab_embed(model, ids, M, h, stream) -> int:

@@ -14,6 +14,8 @@
 #include "tp.h"
 
 namespace tpk {
+bool noalloc_fits(int M, int out_rows, int num_sms, size_t ticket_bytes, size_t partial_bytes,
+                  int max_tokens);
 tp_status row_reduce_in_scratch(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
                                 int64_t x_rank_stride, int64_t ldx, int32_t M,
                                 const tp_bf16* residual, tp_bf16* y, void* scratch,
@@ -39,7 +41,9 @@ constexpr int kMaxDevices = 256;
 void* g_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, resolved once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the life of the
+// process.  A cudaDeviceReset destroys the context the address belongs to,
+// so the entry point must not be called on a device after it was reset.
 tp_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TP_ERR_CUDA;
@@ -64,4 +68,8 @@ extern "C" tp_status tp_row_linear_reduce_noalloc(const tp_model* m, int32_t lay
   return tpk::row_reduce_in_scratch(m, layer, which, x, x_rank_stride, ldx, M, residual, y, scratch,
                                     kTicketBytes, kPartialBytes, kMaxTokens,
                                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int32_t tp_row_linear_reduce_noalloc_fits(int32_t M, int32_t hidden, int32_t num_sms) {
+  return tpk::noalloc_fits(M, hidden, num_sms, kTicketBytes, kPartialBytes, kMaxTokens) ? 1 : 0;
 }

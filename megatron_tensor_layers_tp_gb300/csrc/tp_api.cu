@@ -47,7 +47,7 @@ struct tp_model {
   uint16_t* ones = nullptr;  // [H] bf16 1.0: the norm weight once it is folded
   float2* rope = nullptr;
   int* status = nullptr;
-  std::vector<void*> allocs;
+  std::vector<std::pair<void*, size_t>> allocs;  // device buffers and their sizes
   mutable tp_stats_t stats;
   // per-launch timing (tp_profile)
   bool profiling = false;
@@ -151,7 +151,7 @@ tp_status dev_alloc(tp_model* m, T** p, size_t bytes) {
   void* q = nullptr;
   cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
   if (e != cudaSuccess) return cuda_status(e);
-  m->allocs.push_back(q);
+  m->allocs.push_back({q, bytes});
   *p = static_cast<T*>(q);
   return TP_OK;
 }
@@ -426,6 +426,17 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
   return TP_OK;
 }
 
+// Releases one buffer obtained from dev_alloc (after the stream work that
+// reads it has finished).
+void dev_free(tp_model* m, void* p) {
+  for (size_t i = 0; i < m->allocs.size(); ++i)
+    if (m->allocs[i].first == p) {
+      cudaFree(p);
+      m->allocs.erase(m->allocs.begin() + i);
+      return;
+    }
+}
+
 bool valid_layer(const tp_model* m, int layer) {
   return m && layer >= 0 && layer < (int)m->layers.size();
 }
@@ -529,7 +540,9 @@ tp_status tp_config(tp_config_t* c) {
       !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
     return TP_ERR_ARG;
   const int t = c->t;
-  if (c->attn_dp < 0) return TP_ERR_ARG;
+  if (c->attn_dp < 0 || c->host_io < 0 || c->host_io > 1 || c->plain_column_shards < 0 ||
+      c->plain_column_shards > 1)
+    return TP_ERR_ARG;
   if (c->attn_dp == 0) c->attn_dp = 1;
   if (t % c->attn_dp) return TP_ERR_DIVISIBILITY;
   const int at = t / c->attn_dp;  // attention ranks per DP group
@@ -564,6 +577,14 @@ tp_status tp_config(tp_config_t* c) {
   return TP_OK;
 }
 
+tp_status tp_model_bytes(const tp_model* m, int64_t* bytes) {
+  if (!m || !bytes) return TP_ERR_ARG;
+  int64_t n = 0;
+  for (const auto& a : m->allocs) n += (int64_t)a.second;
+  *bytes = n;
+  return TP_OK;
+}
+
 tp_status tp_get_config(const tp_model* m, tp_config_t* out) {
   if (!m || !out) return TP_ERR_ARG;
   *out = m->cfg;
@@ -573,7 +594,7 @@ tp_status tp_get_config(const tp_model* m, tp_config_t* out) {
 void tp_free(tp_model* m) {
   if (!m) return;
   for (cudaEvent_t e : m->pool) cudaEventDestroy(e);
-  for (void* p : m->allocs) cudaFree(p);
+  for (auto& a : m->allocs) cudaFree(a.first);
   delete m;
 }
 
@@ -637,9 +658,16 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
   if (cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return fail(TP_ERR_CUDA);
   {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrHostNativeAtomicSupported, m->device) == cudaSuccess)
-      m->host_coherent = v != 0;
+    // a coherent host link (NVLink-C2C): native atomics over the link and
+    // pageable host memory reached through the host's page tables; a PCIe
+    // GPU lacks the second, and there zero-copy reads would be slow
+    int atomics = 0, host_pt = 0;
+    if (cudaDeviceGetAttribute(&atomics, cudaDevAttrHostNativeAtomicSupported, m->device) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&host_pt, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                               m->device) != cudaSuccess)
+      return fail(TP_ERR_CUDA);
+    m->host_coherent = atomics != 0 && host_pt != 0 && cfg.host_io == 0;
   }
   // the attention block is sharded over the attn_tp ranks of a DP group, the
   // MLP over all t ranks
@@ -755,17 +783,35 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
         cudaMemcpyAsync(Ls.mlp_norm, Wl.mlp_norm, (size_t)H * 2, cudaMemcpyDeviceToDevice, st) !=
             cudaSuccess)
       return fail(TP_ERR_CUDA);
-    // the norms' weights folded into the column-parallel GEMMs that read them
-    if ((s = alloc_linear(m, &Ls.qkv_folded, nqkv, H, at)) != TP_OK ||
-        (s = alloc_linear(m, &Ls.gate_up_folded, 2 * Ipr, H, t)) != TP_OK)
-      return fail(s);
-    Ls.qkv_folded.bias = Ls.qkv.bias;
-    Ls.gate_up_folded.bias = Ls.gate_up.bias;
-    if (launch_fold_cols(Ls.qkv_folded.data, Ls.qkv.data, Ls.attn_norm, (int64_t)at * nqkv, H, st) !=
-            cudaSuccess ||
-        launch_fold_cols(Ls.gate_up_folded.data, Ls.gate_up.data, Ls.mlp_norm, (int64_t)t * 2 * Ipr,
-                         H, st) != cudaSuccess)
-      return fail(TP_ERR_CUDA);
+    // the norms' weights folded into the column-parallel GEMMs that read them;
+    // a norm weight of exactly 1 leaves the shard unchanged, and then the one
+    // buffer serves the decoder layer and tp_column_linear alike
+    for (int which = 0; which < 2; ++which) {
+      ShardedLinear& plain = which == 0 ? Ls.qkv : Ls.gate_up;
+      ShardedLinear& folded = which == 0 ? Ls.qkv_folded : Ls.gate_up_folded;
+      const uint16_t* nw = which == 0 ? Wl.attn_norm : Wl.mlp_norm;
+      std::vector<uint16_t> hw(H);
+      if (cudaMemcpyAsync(hw.data(), nw, (size_t)H * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        return fail(TP_ERR_CUDA);
+      bool unit = true;
+      for (uint16_t v : hw) unit = unit && v == 0x3F80;  // bf16 1.0
+      if (unit) {
+        folded = plain;
+        continue;
+      }
+      if ((s = alloc_linear(m, &folded, plain.rows, H, plain.ranks)) != TP_OK) return fail(s);
+      folded.bias = plain.bias;
+      if (launch_fold_cols(folded.data, plain.data, nw, (int64_t)plain.ranks * plain.rows, H, st) !=
+          cudaSuccess)
+        return fail(TP_ERR_CUDA);
+      if (!cfg.plain_column_shards) {
+        // tp_column_linear is not served for this layer: drop the unfolded copy
+        if (cudaStreamSynchronize(st) != cudaSuccess) return fail(TP_ERR_CUDA);
+        dev_free(m, plain.data);
+        plain.data = nullptr;
+      }
+    }
   }
   {
     const std::vector<uint16_t> one(H, 0x3F80);  // bf16 1.0
@@ -818,6 +864,7 @@ tp_status tp_column_linear(const tp_model* m, int32_t layer, int32_t which, cons
   if (M == 0) return TP_OK;
   if (!x || !y || !aligned16(x) || !aligned16(y) || y_rank_stride % 8) return TP_ERR_ARG;
   const ShardedLinear& W = which == TP_QKV ? m->layers[layer].qkv : m->layers[layer].gate_up;
+  if (!W.data) return TP_ERR_UNSUPPORTED;  // only the norm-folded shards were kept
   if (y_rank_stride < (int64_t)M * W.rows) return TP_ERR_ARG;
   if (!ws_ok(m, M, ws, ws_bytes)) return TP_ERR_WORKSPACE;
   EpiArgs e = base_epi(m, M);
@@ -1300,6 +1347,21 @@ tp_status tp_check_device(tp_model* m, void* stream) {
 // on `st` before the launch.
 // ============================================================================
 namespace tpk {
+// Whether one fused row-parallel call of M tokens over out_rows output
+// features on a GPU of num_sms SMs fits a fixed scratch of ticket_bytes +
+// partial_bytes: the decode orientation only (M <= max_tokens <=
+// kSwapMaxTokens), one ticket per 128-row output tile, and two fp32 partial
+// tiles of [BN][128] per CTA of the stream-K grid (at most one CTA per SM).
+bool noalloc_fits(int M, int out_rows, int num_sms, size_t ticket_bytes, size_t partial_bytes,
+                  int max_tokens) {
+  if (M < 0 || out_rows < 1 || num_sms < 1 || M > max_tokens || M > kSwapMaxTokens) return false;
+  const GemmPlan p = plan_gemm(std::max(M, 1));
+  if (!p.swap) return false;
+  const size_t tiles = (size_t)cdiv(out_rows, 128);
+  const size_t partials = (size_t)num_sms * 2 * p.BN * 128 * sizeof(float);
+  return tiles * sizeof(int) <= ticket_bytes && partials <= partial_bytes;
+}
+
 tp_status row_reduce_in_scratch(const tp_model* m, int32_t layer, int32_t which, const tp_bf16* x,
                                 int64_t x_rank_stride, int64_t ldx, int32_t M,
                                 const tp_bf16* residual, tp_bf16* y, void* scratch,
@@ -1312,12 +1374,9 @@ tp_status row_reduce_in_scratch(const tp_model* m, int32_t layer, int32_t which,
   if (!x || !y || !aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) ||
       x_rank_stride % 8 || ldx % 8 || ldx < W.cols)
     return TP_ERR_ARG;
-  if (M > max_tokens) return TP_ERR_WORKSPACE;
-  const GemmPlan p = plan_gemm(M);
-  if (!p.swap) return TP_ERR_WORKSPACE;
+  if (!noalloc_fits(M, W.rows, m->num_sms, ticket_bytes, partial_bytes, max_tokens))
+    return TP_ERR_WORKSPACE;
   const size_t tiles = (size_t)cdiv(W.rows, 128);
-  const size_t partials = (size_t)m->num_sms * 2 * p.BN * 128 * sizeof(float);
-  if (tiles * sizeof(int) > ticket_bytes || partials > partial_bytes) return TP_ERR_WORKSPACE;
   TP_CHECK_CUDA(cudaMemsetAsync(scratch, 0, tiles * sizeof(int), st));
   WsLayout L;
   memset(&L, 0, sizeof(L));

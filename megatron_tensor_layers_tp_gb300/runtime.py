@@ -27,12 +27,14 @@ def _stream(stream) -> int:
 
 def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, n_layers, t,
                 rms_eps=1e-5, rope_theta=10000.0, max_positions=8192,
-                attn_dp=1) -> B.tp_config_t:
+                attn_dp=1, host_io=0, plain_column_shards=0) -> B.tp_config_t:
     c = B.tp_config_t()
     c.hidden, c.n_heads, c.n_kv_heads, c.head_dim = hidden, n_heads, n_kv_heads, head_dim
     c.intermediate, c.vocab, c.n_layers, c.t = intermediate, vocab, n_layers, t
     c.rms_eps, c.rope_theta, c.max_positions = rms_eps, rope_theta, max_positions
     c.attn_dp = attn_dp
+    c.host_io = host_io
+    c.plain_column_shards = plain_column_shards
     return c
 
 
@@ -125,6 +127,9 @@ class TPModel:
         c = self.cfg
         return torch.empty((c.kv_copies, n_seqs, c.kv_heads_per_rank, l_max, c.head_dim),
                            dtype=torch.bfloat16, device="cuda")
+
+    def model_bytes(self) -> int:
+        return B.tp_model_bytes(self.handle)
 
     def check_device(self, stream=None) -> int:
         return B.tp_check_device(self.handle, _stream(stream))

@@ -107,3 +107,16 @@ def test_dp_attention_config_rules():
     import oracle as O
     p = O.plan(32, 8, 14336, 1000, O.attn_tp_size(8, 2))
     assert (p.q_heads_per_rank, p.kv_heads_per_rank, p.kv_replicas, p.kv_copies) == (8, 2, 1, 4)
+
+
+def test_noalloc_scratch_limits():
+    # the fixed scratch holds one ticket per 128-row output tile and two fp32
+    # [BN][128] partial tiles per SM: up to 64 tokens, and at 64 tokens
+    # (BN = 64) up to 160 SMs; fewer tokens leave room for more SMs
+    fits = B.tp_row_linear_reduce_noalloc_fits
+    assert fits(1, 4096, 152) == 1 and fits(64, 4096, 152) == 1 and fits(64, 5120, 160) == 1
+    assert fits(65, 4096, 152) == 0            # beyond the decode orientation
+    assert fits(64, 4096, 161) == 0            # 161 x 2 x 64 x 128 x 4 B > 10 MiB
+    assert fits(16, 4096, 161) == 1            # BN = 16: a quarter of the partial bytes
+    assert fits(16, 4096 * 1024 + 128, 152) == 0   # more than 4096 output tiles of tickets
+    assert fits(-1, 4096, 152) == 0 and fits(16, 0, 152) == 0 and fits(16, 4096, 0) == 0

@@ -85,7 +85,7 @@ def test_biased_sharded_equals_unsharded_on_gpu():
 @pytest.mark.parametrize("M", [16, 200])
 def test_column_and_row_calls_carry_their_biases(t, M):
     w = _wl("decode", n_seqs=4, seq_len=1, ctx=8)
-    model, _, _ = build_model(w, t, max_tokens=M)
+    model, _, _ = build_model(w, t, max_tokens=M, plain_column_shards=1)
     W = oracle_layer(w, 0)
     dims = oracle_dims(w)
     p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)

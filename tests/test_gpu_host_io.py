@@ -2,7 +2,9 @@
 the layer on the device, host rows out.  Its result must equal
 tp_layer_forward's bit for bit (same kernels), also when one pinned buffer is
 both input and output over consecutive calls (each call's transfers wait for
-the previous call), and pageable host memory is refused."""
+the previous call), and pageable host memory is refused.  Both transfer
+paths are run: kernels over the coherent host link (GB300) and the copy
+engine (forced with host_io = 1)."""
 import numpy as np
 import pytest
 
@@ -28,28 +30,36 @@ def _hidden(w):
 @pytest.mark.parametrize("mode,n_seqs,seq_len,ctx", [("decode", 16, 1, 300), ("decode", 48, 1, 90),
                                                      ("prefill", 4, 30, 30)])
 @pytest.mark.parametrize("fused,attn_dp", [(True, 1), (False, 1), (True, 2)])
-def test_host_entry_point_equals_device_layer(mode, n_seqs, seq_len, ctx, fused, attn_dp):
+@pytest.mark.parametrize("host_io", [0, 1])
+def test_host_entry_point_equals_device_layer(mode, n_seqs, seq_len, ctx, fused, attn_dp, host_io):
+    # host_io 0: on GB300 the transfers are two kernels over NVLink-C2C;
+    # host_io 1: cudaMemcpyAsync on the stream (the path of other GPUs)
     w = _wl(mode, n_seqs, seq_len, ctx)
-    model, _, _ = build_model(w, 4, attn_dp=attn_dp)
+    model, _, _ = build_model(w, 4, attn_dp=attn_dp, host_io=host_io)
     batch, _ = make_batch(model, w)
     h0 = _hidden(w)
     ref = h0.clone()
+    model.reset_stats()
     model.layer_forward(0, batch, ref, fused=fused)
+    layer_launches = model.stats().kernel_launches
     hin = h0.cpu().pin_memory()
     hout = torch.zeros_like(hin).pin_memory()
     hdev = torch.empty_like(h0)
+    model.reset_stats()
     model.layer_forward_host(0, batch, hin, hout, hdev, fused=fused)
     torch.cuda.synchronize()
     assert model.check_device() == 0
+    assert model.stats().kernel_launches == layer_launches + (2 if host_io == 0 else 0)
     assert torch.equal(hout.view(torch.int16), ref.cpu().view(torch.int16))
     assert torch.equal(hdev.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(hin.view(torch.int16), h0.cpu().view(torch.int16))  # input untouched
     model.close()
 
 
-def test_one_pinned_buffer_through_consecutive_layers():
+@pytest.mark.parametrize("host_io", [0, 1])
+def test_one_pinned_buffer_through_consecutive_layers(host_io):
     w = _wl("decode", 16, 1, 120, layers=3)
-    model, _, _ = build_model(w, 2)
+    model, _, _ = build_model(w, 2, host_io=host_io)
     batch, _ = make_batch(model, w)
     h0 = _hidden(w)
     ref = h0.clone()

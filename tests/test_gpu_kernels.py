@@ -26,7 +26,7 @@ def _wl(hidden=512, n_heads=8, n_kv=2, head_dim=64, inter=1536, vocab=1001, seed
 
 def _model(w, t, head=True):
     cfg = make_config(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab, 1, t,
-                      max_positions=4096)
+                      max_positions=4096, plain_column_shards=1)
     layers = [device_layer(w, 0)]
     emb = lm = fn = None
     if head:

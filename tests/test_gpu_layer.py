@@ -285,17 +285,92 @@ def test_decode_context_edges_match_oracle(t, ctx):
     model.close()
 
 
+def _set_cache_rows(model, cache, rows):
+    """Writes logical cache rows {(b, g, p): values [d]} into the library
+    layout [copies, seqs, kv_r, L, d]: KV head g sits in copy g // kv_r at
+    local index g % kv_r (replica ranks share that copy)."""
+    c = model.cfg
+    for (b, g, p), v in rows.items():
+        cache[g // c.kv_heads_per_rank, b, g % c.kv_heads_per_rank, p] = \
+            torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+
+
 @pytest.mark.parametrize("n_seqs", [6, 64])
-def test_attention_with_dominant_scores_matches_oracle(n_seqs):
-    # cached keys and values ~N(0, 60^2): the scores q.k / sqrt(d) spread over
-    # tens of units, so each softmax is close to one-hot and a slip in the
-    # running maximum or the rescaling of the online softmax shows up at once;
-    # the attention output (values of size ~60) dominates the layer's output.
-    # 6 sequences: each (sequence, KV head) pair's key tiles are split over
-    # several CTAs and combined; 64: whole pairs per CTA
-    w = replace(_wl("decode", n_seqs=n_seqs, seq_len=1, ctx=300, n_kv=2), sigma_kv=60.0)
+def test_attention_with_one_dominant_key_matches_oracle(n_seqs):
+    # In every (sequence, KV head) one cached key points along the group's
+    # queries with a large norm, so its score exceeds every other by more
+    # than 15: the softmax is one-hot to fp32 precision and the attention
+    # output is that position's v.  A slip in the running maximum or in the
+    # rescaling of the online softmax (or of the combine across CTAs) breaks
+    # this at once, while the result stays insensitive to the last-bit
+    # rounding differences of q.  6 sequences: each pair's key tiles are
+    # split over several CTAs and combined; 64: whole pairs per CTA.
+    w = _wl("decode", n_seqs=n_seqs, seq_len=1, ctx=300, n_kv=2)
+    dims = oracle_dims(w)
+    W = oracle_layer(w, 0)
+    h = synth.host_hidden(w)
+    ob = oracle_batch(w)
+    nh, nkv, d = w.n_heads, w.n_kv_heads, w.head_dim
+    group = nh // nkv
+    u = O.round_bf16(O.rmsnorm(h, W.attn_norm, dims.rms_eps))
+    q = O.round_bf16(O.rope(O.linear(u, W.wq).reshape(w.tokens, nh, d), ob.pos, dims.rope_theta))
+    kc, vc = oracle_caches(w, 0, range(n_seqs))
+    rows = {}
+    for b in range(n_seqs):
+        p = (37 * b + 11) % (w.ctx - 1)
+        for g in range(nkv):
+            qg = q[b, g * group:(g + 1) * group]
+            dirn = qg.sum(axis=0)
+            k = O.round_bf16(600.0 * dirn / np.linalg.norm(dirn))
+            kc[b][g, p] = k
+            rows[(b, g, p)] = k
+            s = qg @ kc[b][g, : w.ctx - 1].T / np.sqrt(d)       # the cached keys' scores
+            top = np.sort(s, axis=1)
+            assert np.all(top[:, -1] - top[:, -2] > 15.0)        # one-hot softmax
+            assert np.all(np.argmax(s, axis=1) == p)
+    ref = O.layer_forward(h, W, kc, vc, ob, dims)
     for t in (1, 4):
-        model, h, _ = _run_layer(w, t)
-        ref, _, _ = _oracle_layer(w)
-        assert rel_err(to_f64(h), ref) <= LAYER_TOL, t
+        model, _, _ = build_model(w, t)
+        batch, (ks, vs) = make_batch(model, w)
+        _set_cache_rows(model, ks[0], rows)
+        hd = torch.from_numpy(h.astype(np.float32)).to(torch.bfloat16).cuda()
+        model.layer_forward(0, batch, hd)
+        torch.cuda.synchronize()
+        assert model.check_device() == 0
+        assert rel_err(to_f64(hd), ref) <= LAYER_TOL, t
         model.close()
+
+
+def test_unfolded_shards_kept_only_on_request():
+    # non-unit norm weights: the decoder layer reads the norm-folded qkv and
+    # gate_up shards; the unfolded copies tp_column_linear needs are kept only
+    # with plain_column_shards = 1, and cost exactly their weight bytes
+    w = _wl("decode", n_seqs=4, seq_len=1, ctx=40)
+    outs, sizes = {}, {}
+    for keep in (0, 1):
+        model, _, _ = build_model(w, 2, plain_column_shards=keep)
+        batch, _ = make_batch(model, w)
+        h = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
+        synth.fill_normal_(h, w.seed, synth.tensor_id("hidden"), w.sigma_h)
+        model.layer_forward(0, batch, h)
+        torch.cuda.synchronize()
+        outs[keep], sizes[keep] = h.clone(), model.model_bytes()
+        x = torch.zeros((3, w.hidden), dtype=torch.bfloat16, device="cuda")
+        if keep:
+            model.column_linear(0, B.TP_QKV, x)
+        else:
+            with pytest.raises(B.TPError) as ei:
+                model.column_linear(0, B.TP_QKV, x)
+            assert ei.value.status == B.STATUS["TP_ERR_UNSUPPORTED"]
+        model.close()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    d = w.head_dim
+    plain = ((w.n_heads + 2 * w.n_kv_heads) * d + 2 * w.intermediate) * w.hidden * 2
+    assert sizes[1] - sizes[0] == plain
+    # unit norm weights: folded and unfolded shards are the same buffer
+    wu = replace(w, norm_weight_sigma=0.0)
+    m0, _, _ = build_model(wu, 2, plain_column_shards=0)
+    m1, _, _ = build_model(wu, 2, plain_column_shards=1)
+    assert m0.model_bytes() == m1.model_bytes()
+    m0.column_linear(0, B.TP_GATE_UP, torch.zeros((3, w.hidden), dtype=torch.bfloat16, device="cuda"))
+    m0.close(); m1.close()
