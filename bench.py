@@ -130,6 +130,73 @@ def read_peaks():
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
+class NvmlSampler:
+    """Reads the SM clock and the clock-event reasons through NVML (ctypes,
+    read-only queries) every ~0.5 ms from a thread, so that even a timed
+    region of a few milliseconds holds samples.  Raises OSError when NVML is
+    not available (the nvidia-smi sampler is used then)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(gpu_index, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.on = False
+        self.stop_flag = False
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct, lib = self.ct, self.lib
+        mhz, rs, mw = ct.c_uint(0), ct.c_ulonglong(0), ct.c_uint(0)
+        while not self.stop_flag:
+            if self.on:
+                lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))
+                lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, ct.byref(rs))
+                lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+                self.samples.append((float(mhz.value), int(rs.value), mw.value / 1000.0))
+            time.sleep(0.0005)
+
+    def start(self):
+        self.on = True
+
+    def stop(self):
+        self.on = False
+        self.stop_flag = True
+        self.thread.join(timeout=2)
+
+    def summary(self, *_):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml"}
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(m for m, _, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "power_w_max": max(p for _, _, p in self.samples),
+                "samples": len(self.samples), "source": "nvml, every ~0.5 ms inside the timed region"}
+
+
+def clock_sampler(gpu_index: int):
+    try:
+        return NvmlSampler(gpu_index)
+    except (OSError, AttributeError):
+        return ClockSampler(gpu_index)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -154,6 +221,9 @@ class ClockSampler:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
                 self.samples.append((time.time(), parts))
+
+    def start(self):
+        pass
 
     def stop(self):
         if self.proc:
@@ -271,6 +341,26 @@ def timed_steps(model, batch, h, steps, warmup, rotate, fused, stream, profile=F
     return ms, prof, launches
 
 
+def step_median_ms(model, batch, h, steps, rotate, fused, stream):
+    """Median of per-step CUDA-event durations (events recorded between the
+    steps on the launch stream), in a pass of its own: an event between two
+    steps ends the programmatic overlap of the steps' kernels, so this pass
+    stays out of the headline window."""
+    import torch
+    from megatron_tensor_layers_tp_gb300 import binding as B
+    cb = batch.to_c()
+    ws, nws = model.ws_args
+    s = stream.cuda_stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        B.check(B.tp_layer_forward(model.handle, i % rotate, cb, h.data_ptr(), fused, ws, nws, s),
+                "tp_layer_forward")
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -288,41 +378,37 @@ def run_ours(args, rank, world):
             gpu_idx = int(vis.split(",")[gpu_idx])
         except ValueError:
             pass
-    sampler = ClockSampler(gpu_idx)
+    sampler = clock_sampler(gpu_idx)
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_host0 = time.time()
+    sampler.start()
     ms, _, launches = timed_steps(model, batch, h, args.steps, args.warmup, args.rotate,
                                   args.fused, stream, profile=False)
+    sampler.stop()
     t_host1 = time.time()
     if world > 1:
         dist.barrier()
-    sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
+    ms = max_over_ranks(ms, world)
+    med_steps = max(20, min(args.steps, 200))
+    ms_med = step_median_ms(model, batch, h, med_steps, args.rotate, args.fused, stream)
     # per-kernel durations: the same steps again with two CUDA events recorded
     # around every launch on the launch stream (the brackets cost a few
     # microseconds per launch, so they stay out of the headline region)
     prof_steps = min(args.steps, 2000)
     ms_prof, prof, _ = timed_steps(model, batch, h, prof_steps, 0, args.rotate, args.fused,
                                    stream, profile=True)
-    ms = max_over_ranks(ms, world)
     assert model.check_device(stream) == 0, "device status word set"
     ms_step = ms / args.steps
     tokens = w.tokens
     value = whole_job_rate(tokens, args.steps, ms, world)
+    model_bytes_per_layer = model.model_bytes() / args.rotate
 
     kb, step_bytes = layer_bytes(w, args.t)
-    kernels = {}
-    for name, (n, tot) in prof.items():
-        avg = tot / n
-        entry = {"launches": n, "avg_us": round(avg * 1e3, 2),
-                 "share": None}
-        if name in kb:
-            entry["gbs"] = round(kb[name] / (avg * 1e-3) / 1e9, 1)
-            entry["frac_hbm"] = round(entry["gbs"] / hbm_peak, 3)
-        kernels[name] = entry
+    kernels = kernel_table(prof, kb, hbm_peak)
     tot_all = sum(tot for _, tot in prof.values()) or 1.0
     for name, (n, tot) in prof.items():
         kernels[name]["share"] = round(tot / tot_all, 3)
@@ -355,32 +441,31 @@ def run_ours(args, rank, world):
     for g in graphs:
         g.close()
 
-    # t = 1, 2, 4 beside the headline
+    # every t, with the fused and the unfused reduction (the unfused one
+    # materialises t fp32 partials per row-parallel op and reduces them in a
+    # kernel of its own: its extra HBM cost is the measured difference)
     per_t = {}
     if args.per_t and rank == 0 and world == 1:
-        per_t[str(args.t)] = {"tokens_per_s": round(value, 1), "ms_per_step": round(ms_step, 4),
-                              "step_hbm_frac": round(step_gbs / hbm_peak, 3)}
-        for tt in (1, 2, 4):
+        n_pt = max(args.steps // 4, 20)
+
+        def one(m_, b_, h_, tt, fused):
+            ms_, _, _ = timed_steps(m_, b_, h_, n_pt, args.warmup, args.rotate, fused, stream)
+            st_ = ms_ / n_pt
+            _, sb_ = layer_bytes(w, tt)
+            return {"ms": round(st_, 4), "tok_s": round(tokens / (st_ * 1e-3)),
+                    "hbm_frac": round(sb_ / (st_ * 1e-3) / 1e9 / hbm_peak, 3)}
+        for tt in (1, 2, 4, 8):
             if tt == args.t:
-                continue
-            with torch.cuda.stream(stream):
-                m2, b2, h2 = build(w, tt, args.rotate)
-            ms2, _, _ = timed_steps(m2, b2, h2, max(args.steps // 4, 20), args.warmup, args.rotate,
-                                    args.fused, stream)
-            st2 = ms2 / max(args.steps // 4, 20)
-            _, sb2 = layer_bytes(w, tt)
-            per_t[str(tt)] = {"tokens_per_s": round(tokens / (st2 * 1e-3), 1),
-                              "ms_per_step": round(st2, 4),
-                              "step_hbm_frac": round(sb2 / (st2 * 1e-3) / 1e9 / hbm_peak, 3)}
-            m2.close()
-            del m2, b2, h2
-        # the unfused reduction variant at the headline t
-        ms_u, _, _ = timed_steps(model, batch, h, max(args.steps // 4, 20), args.warmup,
-                                 args.rotate, 0, stream)
-        per_t[f"{args.t}_unfused"] = {
-            "tokens_per_s": round(tokens / (ms_u / max(args.steps // 4, 20) * 1e-3), 1),
-            "ms_per_step": round(ms_u / max(args.steps // 4, 20), 4),
-            "extra_partial_bytes_per_row_op": 2 * args.t * w.tokens * w.hidden * 4}
+                m2, b2, h2 = model, batch, h
+            else:
+                with torch.cuda.stream(stream):
+                    m2, b2, h2 = build(w, tt, args.rotate)
+            per_t[str(tt)] = {"fused": one(m2, b2, h2, tt, 1), "unfused": one(m2, b2, h2, tt, 0),
+                              "unfused_extra_bytes_per_row_op": 2 * tt * w.tokens * w.hidden * 4}
+            if m2 is not model:
+                m2.close()
+                del m2, b2, h2
+                torch.cuda.empty_cache()
 
     # end to end through the public API with host buffers: each step, the
     # library's host-buffer call brings the pinned input rows to the device,
@@ -423,21 +508,28 @@ def run_ours(args, rank, world):
     cpu = None
     if args.cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(w, args.t, args.cpu_budget_s)
-    prefill = None
-    configs = {}
+    prefill = prefill_detail = None
+    configs, configs_detail = {}, {}
     if (args.prefill or args.configs) and rank == 0 and world == 1:
         model.close()
         torch.cuda.empty_cache()
     if args.prefill and rank == 0 and world == 1:
-        prefill = prefill_section(stream)
+        prefill, prefill_detail = prefill_section(stream)
     if args.configs and rank == 0 and world == 1:
         for name in ("qwen32b_decode", "qwen32b_decode_kv4"):
-            configs[name] = decode_layer_section(name, stream, hbm_peak)
-        configs["llama8b_full"] = full_forward_section(stream, hbm_peak)
+            configs[name], configs_detail[name] = decode_layer_section(name, stream, hbm_peak)
+        configs["llama8b_full"], configs_detail["llama8b_full"] = full_forward_section(stream, hbm_peak)
 
     model.close()
     if rank != 0:
         return
+    # per-kernel tables of every section: a second JSON line on stderr
+    print(json.dumps({"bench_detail": {"decode_layer_kernels": kernels, "prefill": prefill_detail,
+                                       "decode_configs": configs_detail,
+                                       "kernel_timing": "CUDA events around each launch on the "
+                                       f"launch stream, {prof_steps} steps after the timed region "
+                                       f"({ms_prof / prof_steps:.4f} ms/step with the events)"}}),
+          file=sys.stderr, flush=True)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -453,18 +545,20 @@ def run_ours(args, rank, world):
             "l2": f"inputs larger than L2: steps rotate over {args.rotate} layers with distinct "
                   f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
             "step_bytes": step_bytes, "step_gbs": round(step_gbs, 1),
-            "ms_per_step_cuda_graph": round(ms_graph_step, 5),
             "step_hbm_frac": round(step_gbs / hbm_peak, 3),
-            "per_t": per_t, "kernels": kernels, "prefill": prefill, "decode_configs": configs,
-            "kernel_timing": f"CUDA events around each launch on the launch stream, {prof_steps} "
-                             f"steps right after the timed region ({ms_prof / prof_steps:.4f} "
-                             "ms/step with the events)",
+            "ms_per_step_median": round(ms_med, 5), "median_of_steps": med_steps,
+            "ms_per_step_cuda_graph": round(ms_graph_step, 5),
+            "model_bytes_per_layer": int(model_bytes_per_layer),
+            "kernels_per_step": round(launches / args.steps, 2),
         },
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
+        "decode_configs": configs,
+        "prefill": prefill,
+        "per_t": per_t,
     }
     print(json.dumps(line), flush=True)
 
@@ -475,7 +569,8 @@ def kernel_table(prof, kb, hbm_peak):
         avg = tot / n
         e = {"launches": n, "avg_us": round(avg * 1e3, 2)}
         if name in kb:
-            e["frac_hbm"] = round(kb[name] / (avg * 1e-3) / 1e9 / hbm_peak, 3)
+            e["gbs"] = round(kb[name] / (avg * 1e-3) / 1e9, 1)
+            e["frac_hbm"] = round(e["gbs"] / hbm_peak, 3)
         out[name] = e
     return out
 
@@ -499,12 +594,12 @@ def decode_layer_section(name, stream, hbm_peak, steps=200, warmup=10):
     torch.cuda.empty_cache()
     kb, step_bytes = layer_bytes(w, t)
     st = ms / steps
-    return {"workload": f"Qwen2.5-32B-shaped decoder layer, decode: {w.n_seqs} sequences x 1 token, "
-                        f"{w.ctx}-token KV context, {w.n_kv_heads} KV heads, t={t}",
-            "tokens_per_s": round(w.tokens / (st * 1e-3), 1), "ms_per_step": round(st, 4),
-            "step_bytes": step_bytes,
-            "step_hbm_frac": round(step_bytes / (st * 1e-3) / 1e9 / hbm_peak, 3),
-            "kernels": kernel_table(prof, kb, hbm_peak)}
+    compact = {"ms": round(st, 4), "tok_s": round(w.tokens / (st * 1e-3)),
+               "hbm_frac": round(step_bytes / (st * 1e-3) / 1e9 / hbm_peak, 3)}
+    detail = {"workload": f"Qwen2.5-32B-shaped decoder layer, decode: {w.n_seqs} sequences x 1 "
+                          f"token, {w.ctx}-token KV context, {w.n_kv_heads} KV heads, t={t}",
+              "step_bytes": step_bytes, **compact, "kernels": kernel_table(prof, kb, hbm_peak)}
+    return compact, detail
 
 
 def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
@@ -561,21 +656,23 @@ def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
     kb["gemm_lm_head"] = w.vocab * w.hidden * 2 + w.tokens * w.hidden * 2 + w.tokens * w.vocab * 2
     kb["embed"] = 2 * w.tokens * w.hidden * 2
     step_bytes = w.n_layers * lb + kb["gemm_lm_head"] + kb["embed"]  # norms: see layer_bytes
-    return {"workload": "Llama-3.1-8B-shaped full decode forward: 64 sequences x 1 token, 4096-token "
-                        "KV context, 32 layers + embedding + LM head, t=8",
-            "tokens_per_s": round(w.tokens / (ms * 1e-3), 1), "ms_per_forward": round(ms, 4),
-            "ms_per_forward_cuda_graph": round(ms_graph, 4),
-            "step_bytes": step_bytes,
-            "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
-            "kernels": kernel_table(prof, kb, hbm_peak)}
+    compact = {"ms": round(ms, 4), "tok_s": round(w.tokens / (ms * 1e-3)),
+               "hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
+               "ms_cuda_graph": round(ms_graph, 4)}
+    detail = {"workload": "Llama-3.1-8B-shaped full decode forward: 64 sequences x 1 token, "
+                          "4096-token KV context, 32 layers + embedding + LM head, t=8",
+              "step_bytes": step_bytes, **compact, "kernels": kernel_table(prof, kb, hbm_peak)}
+    return compact, detail
 
 
 def prefill_section(stream, reps=10):
     """Llama-3.1-8B-shaped prefill chunk at t = 4: 8 sequences x 256 tokens
     through the vocab-parallel embedding, one decoder layer and the
     vocab-parallel LM head on each sequence's last token.  Reports every
-    kernel's duration and, for the contractions, TFLOP/s against the sustained
-    bf16 tensor-core peak (the GEMMs run inside a multi-kernel step)."""
+    kernel's duration and, for the contractions, TFLOP/s against the burst
+    bf16 tensor-core peak (each forward lasts under a millisecond and the
+    timed loop ten of them: far from the seconds-long loop of the sustained
+    figure)."""
     import torch
     import synth
     from megatron_tensor_layers_tp_gb300 import binding as B
@@ -629,10 +726,6 @@ def prefill_section(stream, reps=10):
     prof = B.tp_profile_read(model.handle, stream.cuda_stream)
     assert model.check_device(stream) == 0
     _, tc_peak, _ = read_peaks()
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    sustained = tc_peak
-    if os.path.exists(pk_path):
-        sustained = json.load(open(pk_path)).get("bf16_tflops_sustained", tc_peak)
     attn_flops = 0
     for _ in range(w.n_seqs):
         attn_flops += 4 * w.n_heads * d * (w.seq_len * (w.seq_len + 1) // 2)
@@ -650,7 +743,7 @@ def prefill_section(stream, reps=10):
         if name in flops:
             tf = flops[name] / (avg_ms * 1e-3) / 1e12
             e["tflops"] = round(tf, 1)
-            e["frac_tc_sustained"] = round(tf / sustained, 3)
+            e["frac_tc"] = round(tf / tc_peak, 3)
         if name == "gemm_lm_head":
             gbs = (V * H * 2) / (avg_ms * 1e-3) / 1e9
             e["gbs"] = round(gbs, 1)
@@ -659,12 +752,17 @@ def prefill_section(stream, reps=10):
     g_flops = sum(flops[k] for k in gem)
     g_ms = sum(prof[k][1] / prof[k][0] for k in gem)
     model.close()
-    return {"workload": "8 sequences x 256 tokens, t=4: embedding + 1 layer + LM head on the last "
-                        "token of each sequence", "ms_per_forward": round(ms, 4),
-            "tokens_per_s": round(M / (ms * 1e-3), 1),
-            "gemm_tflops": round(g_flops / (g_ms * 1e-3) / 1e12, 1),
-            "gemm_frac_tc_sustained": round(g_flops / (g_ms * 1e-3) / 1e12 / sustained, 3),
-            "tc_peak_sustained": sustained, "kernels": kern}
+    tot = sum(p[1] for p in prof.values()) / reps
+    compact = {"ms": round(ms, 4), "tok_s": round(M / (ms * 1e-3)),
+               "gemm_frac_tc": round(g_flops / (g_ms * 1e-3) / 1e12 / tc_peak, 3),
+               "tc_peak": tc_peak,
+               **{k[5:]: kern[k]["frac_tc"] for k in gem},
+               "attn_us": kern.get("attn_prefill", {}).get("avg_us"),
+               "attn_share": round(prof["attn_prefill"][1] / reps / tot, 3) if "attn_prefill" in prof else None}
+    detail = {"workload": "8 sequences x 256 tokens, t=4: embedding + 1 layer + LM head on the "
+                          "last token of each sequence", **compact,
+              "gemm_tflops": round(g_flops / (g_ms * 1e-3) / 1e12, 1), "kernels": kern}
+    return compact, detail
 
 
 # ---------------------------------------------------------------------------
@@ -752,7 +850,7 @@ def main():
     if args.prefill_only:
         import torch
         stream = torch.cuda.Stream()
-        print(json.dumps({"prefill": prefill_section(stream)}), flush=True)
+        print(json.dumps({"prefill": prefill_section(stream)[1]}), flush=True)
         return
     if world > 1:
         import torch
