@@ -298,15 +298,13 @@ EpiArgs base_epi(const tp_model* m, int M) {
 }
 
 // Column-parallel family (qkv, gate_up, LM head): each rank r produces its own
-// [M, rows] output from the replicated x [M, K].
-tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W,
-                     const uint16_t* x, int64_t ldx, int M, int epi, const EpiArgs& e, void* ws,
-                     const WsLayout& L, cudaStream_t st) {
-  if (M == 0) return TP_OK;
-  const tp_config_t& c = m->cfg;
+// [M, rows] output from the replicated x [M, K].  Fills the arguments and the
+// schedule of one GEMM launch.
+tp_status prep_column(const tp_model* m, const ShardedLinear& W, const uint16_t* x, int64_t ldx,
+                      int M, int epi, const EpiArgs& e, void* ws, const WsLayout& L, GemmArgs& a,
+                      GemmPlan& p) {
   const int K = W.cols;
-  GemmPlan p = plan_gemm(M);
-  GemmArgs a;
+  p = plan_gemm(M);
   memset(&a, 0, sizeof(a));
   bool ok;
   if (p.swap) {
@@ -344,21 +342,30 @@ tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W
   a.e = e;
   a.e.bias = W.bias;  // rank g's rows carry their own bias entries
   a.e.bias_group_stride = W.rows;
+  return TP_OK;
+}
+
+tp_status run_column(const tp_model* m, const char* name, const ShardedLinear& W,
+                     const uint16_t* x, int64_t ldx, int M, int epi, const EpiArgs& e, void* ws,
+                     const WsLayout& L, cudaStream_t st) {
+  if (M == 0) return TP_OK;
+  GemmArgs a;
+  GemmPlan p;
+  tp_status s = prep_column(m, W, x, ldx, M, epi, e, ws, L, a, p);
+  if (s != TP_OK) return s;
   return cuda_status(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
 }
 
 // Row-parallel family (o_proj, down_proj): rank r holds W_r [H, K_r] and reads
 // x_r [M, K_r]; fused = sum over ranks inside the GEMM (epilogue EPI_RESID),
 // otherwise per-rank fp32 partials then the ordered reduction kernel.
-tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, const uint16_t* x,
-                  int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
-                  uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st,
-                  float* sq_out = nullptr) {
-  if (M == 0) return TP_OK;
+tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
+                   int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
+                   uint16_t* y, int fused, void* ws, const WsLayout& L, float* sq_out,
+                   GemmArgs& a, GemmPlan& p, int& epi) {
   const tp_config_t& c = m->cfg;
   const int Kr = W.cols, H = W.rows, t = W.ranks;
-  GemmPlan p = plan_gemm(M);
-  GemmArgs a;
+  p = plan_gemm(M);
   memset(&a, 0, sizeof(a));
   const uint64_t xs_bytes = (uint64_t)x_rank_stride * 2;
   bool ok;
@@ -388,7 +395,6 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
   a.e = base_epi(m, M);
-  int epi;
   float* rp = at<float>(ws, L.rank_partials);
   if (fused) {
     a.n_groups = 1;
@@ -415,6 +421,21 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
     epi = EPI_PARTIAL;
   }
   set_schedule(a, p, m->num_sms, epi);
+  return TP_OK;
+}
+
+tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, const uint16_t* x,
+                  int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
+                  uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st,
+                  float* sq_out = nullptr) {
+  if (M == 0) return TP_OK;
+  const int H = W.rows, t = W.ranks;
+  GemmArgs a;
+  GemmPlan p;
+  int epi = 0;
+  tp_status s = prep_row(m, W, x, x_rank_stride, ldx, M, residual, y, fused, ws, L, sq_out, a, p, epi);
+  if (s != TP_OK) return s;
+  float* rp = at<float>(ws, L.rank_partials);
   TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
   if (!fused) {
     TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {
@@ -953,6 +974,80 @@ static tp_status check_batch(const tp_model* m, const tp_batch_t* b) {
   return TP_OK;
 }
 
+// Arguments of the decode / prefill attention over the batch's caches; the
+// decode grid is chosen for num_ctas SMs.
+static tp_status prep_attention(const tp_model* m, const tp_batch_t* b, uint16_t* kc, uint16_t* vc,
+                                const uint16_t* q, uint16_t* o, void* ws, const WsLayout& L,
+                                int num_ctas, AttnArgs& a) {
+  const tp_config_t& c = m->cfg;
+  const int d = c.head_dim, nhd = c.n_heads * d;
+  memset(&a, 0, sizeof(a));
+  const uint64_t slices = (uint64_t)c.kv_copies * b->n_seqs * c.kv_heads_per_rank;
+  if (!make_tmap(&a.tmK, kc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64) ||
+      !make_tmap(&a.tmV, vc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64))
+    return TP_ERR_CUDA;
+  a.q = q;
+  a.ld_q = nhd;
+  a.o = o;
+  a.ld_o = nhd;
+  a.positions = b->positions;
+  a.seq_start = b->seq_start;
+  a.n_seqs = b->n_seqs;
+  a.n_heads = c.n_heads;
+  a.n_kv = c.n_kv_heads;
+  a.head_dim = d;
+  a.kv_r = c.kv_heads_per_rank;
+  a.group = c.n_heads / c.n_kv_heads;
+  a.l_max = b->l_max;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  a.status = m->status;
+  if (b->mode == TP_DECODE) {
+    a.tiles_per_bg = cdiv(b->max_ctx, 64);
+    a.total_units = (int64_t)b->n_seqs * c.n_kv_heads * a.tiles_per_bg;
+    // Whole (sequence, KV head) pairs per CTA when they can be dealt out
+    // evenly to at least 80% of the SMs and a CTA's share stays within
+    // kAttnWholeMaxTiles key tiles: no pair is then split and no partial
+    // result needs combining.  Otherwise split the flat range evenly over the
+    // SMs (measured: whole pairs win by 8.5 us at 16 tiles per CTA and by
+    // 4.5 us at 64, tie at 128, and lose by 4 us at 256, where the longer
+    // streams amortise the combine).
+    const int64_t n_bg = (int64_t)b->n_seqs * c.n_kv_heads;
+    int grid = (int)std::min<int64_t>(num_ctas, a.total_units);
+    for (int64_t dd = 1; dd <= n_bg; ++dd) {
+      if (n_bg % dd) continue;
+      const int64_t g = n_bg / dd;
+      if (g <= num_ctas) {
+        if (g * 5 >= (int64_t)num_ctas * 4 && dd * a.tiles_per_bg <= kAttnWholeMaxTiles)
+          grid = (int)g;
+        break;
+      }
+    }
+    a.grid = grid;
+    a.partials = at<float>(ws, L.attn_partials);
+    a.tickets = at<int>(ws, L.attn_tickets);
+  }
+  return TP_OK;
+}
+
+// The epilogue arguments of the qkv projection: RoPE, q into its buffer, the
+// new K/V rows into the rank caches.
+static EpiArgs qkv_epi(const tp_model* m, const tp_batch_t* b, int M, uint16_t* q, uint16_t* kc,
+                       uint16_t* vc) {
+  const tp_config_t& c = m->cfg;
+  EpiArgs e = base_epi(m, M);
+  e.out = q;
+  e.ld_out = c.n_heads * c.head_dim;
+  e.k_cache = kc;
+  e.v_cache = vc;
+  e.kv_copy_stride = (int64_t)b->n_seqs * c.kv_heads_per_rank * b->l_max * c.head_dim;
+  e.n_seqs = b->n_seqs;
+  e.l_max = b->l_max;
+  e.positions = b->positions;
+  e.token_seq = b->token_seq;
+  e.rope = m->rope;
+  return e;
+}
+
 // h_sq: on entry, whether the sums of squares of h's rows sit in the
 // workspace (the previous layer's down_proj left them); on exit, whether this
 // layer's down_proj left them for the next.
@@ -1003,66 +1098,14 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   };
   const uint16_t* xin = nullptr;
   // qkv (column-parallel) + RoPE + K/V into the rank caches
-  EpiArgs e = base_epi(m, M);
+  EpiArgs e = qkv_epi(m, b, M, q, kc, vc);
   if ((s = norm_in(e, *h_sq, &xin)) != TP_OK) return s;
-  e.out = q;
-  e.ld_out = nhd;
-  e.k_cache = kc;
-  e.v_cache = vc;
-  e.kv_copy_stride = (int64_t)b->n_seqs * c.kv_heads_per_rank * b->l_max * d;
-  e.n_seqs = b->n_seqs;
-  e.l_max = b->l_max;
-  e.positions = b->positions;
-  e.token_seq = b->token_seq;
-  e.rope = m->rope;
   if ((s = run_column(m, "gemm_qkv", Ls.qkv_folded, xin, H, M, EPI_QKV, e, ws, L, st)) != TP_OK)
     return s;
   // attention
   AttnArgs a;
-  memset(&a, 0, sizeof(a));
-  const uint64_t slices = (uint64_t)c.kv_copies * b->n_seqs * c.kv_heads_per_rank;
-  if (!make_tmap(&a.tmK, kc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64) ||
-      !make_tmap(&a.tmV, vc, d, b->l_max, slices, (uint64_t)d * 2, (uint64_t)b->l_max * d * 2, 64))
-    return TP_ERR_CUDA;
-  a.q = q;
-  a.ld_q = nhd;
-  a.o = o;
-  a.ld_o = nhd;
-  a.positions = b->positions;
-  a.seq_start = b->seq_start;
-  a.n_seqs = b->n_seqs;
-  a.n_heads = c.n_heads;
-  a.n_kv = c.n_kv_heads;
-  a.head_dim = d;
-  a.kv_r = c.kv_heads_per_rank;
-  a.group = c.n_heads / c.n_kv_heads;
-  a.l_max = b->l_max;
-  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  a.status = m->status;
+  if ((s = prep_attention(m, b, kc, vc, q, o, ws, L, m->num_sms, a)) != TP_OK) return s;
   if (b->mode == TP_DECODE) {
-    a.tiles_per_bg = cdiv(b->max_ctx, 64);
-    a.total_units = (int64_t)b->n_seqs * c.n_kv_heads * a.tiles_per_bg;
-    // Whole (sequence, KV head) pairs per CTA when they can be dealt out
-    // evenly to at least 80% of the SMs and a CTA's share stays within
-    // kAttnWholeMaxTiles key tiles: no pair is then split and no partial
-    // result needs combining.  Otherwise split the flat range evenly over the
-    // SMs (measured: whole pairs win by 8.5 us at 16 tiles per CTA and by
-    // 4.5 us at 64, tie at 128, and lose by 4 us at 256, where the longer
-    // streams amortise the combine).
-    const int64_t n_bg = (int64_t)b->n_seqs * c.n_kv_heads;
-    int grid = (int)std::min<int64_t>(m->num_sms, a.total_units);
-    for (int64_t d = 1; d <= n_bg; ++d) {
-      if (n_bg % d) continue;
-      const int64_t g = n_bg / d;
-      if (g <= m->num_sms) {
-        if (g * 5 >= (int64_t)m->num_sms * 4 && d * a.tiles_per_bg <= kAttnWholeMaxTiles)
-          grid = (int)g;
-        break;
-      }
-    }
-    a.grid = grid;
-    a.partials = at<float>(ws, L.attn_partials);
-    a.tickets = at<int>(ws, L.attn_tickets);
     TP_CHECK_CUDA(launch(m, "attn_decode", st, [&] { return launch_attn_decode(a, st); }));
   } else {
     const int nqb = cdiv(b->max_q_per_seq, 64);
