@@ -27,6 +27,7 @@
 #include "attn_tile.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "rms.cuh"
 
 namespace tpk {
 
@@ -49,15 +50,37 @@ struct DecSmem {
   // (stage n % S, group n % 2 relative to the segment's first unit), so a
   // group never waits on a stage whose previous fill, owned by the other
   // group, is still in flight (an mbarrier parity wait cannot tell that fill
-  // from the one it wants).
-  static constexpr int kStages = D == 128 ? 4 : 8;
-  static_assert(kStages % kDecGroups == 0, "stages must split evenly between the warp groups");
-  // combine rows: O, m, l per warp/row; the pitch keeps the two rows a warp
+  // from the one it wants).  The host takes the largest even count up to
+  // kMaxStages that fits next to the combine buffer.
+  static constexpr int kMaxStages = 8;
+  // combine rows: O, m, l of every warp for each of the KV head's query rows
+  // (n_heads / n_kv of the 16 MMA rows); the pitch keeps the two rows a warp
   // reads at once 18 banks apart (16 lanes per row, columns lane + 16 j)
   static constexpr int kCombLd = D + 18;
-  static constexpr int kComb = kDecWarps * 16 * kCombLd;  // floats
-  static constexpr size_t bytes(int) {
-    return 1024 + (size_t)kStages * kStageBytes + 16 * kQRow + (size_t)kComb * 4 + 256;
+  struct Layout {
+    size_t tiles, sq, comb, bars, misc, knew, total;
+  };
+  __host__ __device__ static constexpr Layout layout(int stages, int rows) {
+    Layout L{};
+    size_t off = 0;
+    L.tiles = off;
+    off += (size_t)stages * kStageBytes;
+    L.sq = off;
+    off += 16 * kQRow;
+    L.comb = off;  // also the deferred qkv's unscaled sums before the tile loop
+    off += (size_t)kDecWarps * rows * kCombLd * 4;
+    off = (off + 15) & ~(size_t)15;
+    L.bars = off;
+    off += 2 * kMaxStages * 8;
+    L.misc = off;
+    off += 64;     // flag, the prologue's per-warp sums, the token's 1/rms
+    L.knew = off;
+    off += 2 * D * 4;
+    L.total = off + 1024;
+    return L;
+  }
+  __host__ __device__ static constexpr size_t bytes(int stages, int rows) {
+    return layout(stages, rows).total;
   }
 };
 
@@ -70,21 +93,206 @@ __device__ __forceinline__ void store_out_row(uint16_t* dst, const float (&v)[N]
   for (int j = 0; j < N; ++j) dst[16 * j] = f_to_bf16(v[j] * inv);
 }
 
+// The 1/rms of token b for the RMSNorm folded into the qkv weights, by the
+// 256 consumer threads (red: 8 floats of shared scratch): from the token's
+// hidden row (norm_mode 1), from the partial sums of squares the kernel that
+// wrote the row left (norm_mode 2), or 1 (norm_mode 0: the GEMM read the
+// normalised rows).  Reads only what earlier kernels wrote, so it may run
+// before the dependency wait on the qkv GEMM.
+template <int D>
+__device__ float token_rs(const AttnArgs& a, int b, float* red) {
+  const int ctid = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NT = kDecWarps * 32;
+  if (a.norm_mode == 0) return 1.f;
+  float ss = 0.f;
+  if (a.norm_mode == 1) {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.norm_src + (int64_t)b * a.norm_ld);
+    const int nv = a.norm_width >> 3;
+    uint4 hv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      hv[k] = ctid + k * NT < nv ? __ldcg(xr + ctid + k * NT) : make_uint4(0, 0, 0, 0);
+    auto add_sq = [&](const uint4& p) {
+      const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    };
+#pragma unroll
+    for (int k = 0; k < 4; ++k) add_sq(hv[k]);
+    for (int v = ctid + 4 * NT; v < nv; v += NT) add_sq(__ldcg(xr + v));
+  } else {
+    const float4* pr = reinterpret_cast<const float4*>(a.norm_partials + (int64_t)b * a.norm_slots);
+    for (int i4 = ctid; i4 < (a.norm_slots >> 2); i4 += NT) {
+      const float4 p = __ldcg(pr + i4);
+      ss += (p.x + p.y) + (p.z + p.w);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  bar_sync(1, NT);
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) t += red[w];
+  bar_sync(1, NT);  // red is reused
+  return 1.0f / sqrtf(t / (float)a.norm_width + a.norm_eps);
+}
+
+// Deferred qkv epilogue of one (sequence b, KV head g): the qkv GEMM left
+// stream-K pieces of fp32 accumulators; sum the pieces of every q row of the
+// group's query heads and of the K and V rows of head g at token b, in K
+// order, then do what the GEMM epilogue would have done: scale by the token's
+// 1/rms rs (the norm weight is folded into the weights), add the bias, rotate
+// the RoPE pairs (shard rows 2i, 2i+1 hold features i and i + d/2 of a Q or K
+// head), round to bf16.  q goes to the CTA's query rows sQ, k and v to knew /
+// vnew; `write` also stores the new K/V row into the cache at the token's
+// position.  All 256 consumer threads take part, two items (row pairs) per
+// thread per round; every load of a round (the pieces, the RoPE factors, the
+// biases) is issued before any is used, so a round costs one trip to L2.
+template <int D>
+__device__ void qkv_from_pieces(const AttnArgs& a, int b, int g, int pos, float rs, bool write,
+                                uint8_t* sQ, int qrow_bytes, float* knew, float* vnew) {
+  const int ctid = threadIdx.x;
+  constexpr int NT = kDecWarps * 32;
+  constexpr int kMaxPieces = 6;  // pieces loaded together per row pair
+  const int half = D / 2, nq = a.q_per_rank, kvr = a.kv_r;
+  const int kv_rank = a.kv_replicas == 1 ? g / kvr : g * a.kv_replicas;  // first holder of head g
+  const int kv_local = g % kvr;
+  const int n_items = (a.group + 2) * half;
+  const bool pos_ok = pos >= 0 && pos < a.l_max;
+  // (32-bit piece arithmetic: the host keeps pc_total * pc_grid below 2^31)
+  const int T = static_cast<int>(a.pc_total), Gp = a.pc_grid, K = a.pc_k;
+  const int64_t piece = (int64_t)a.pc_bn * 128;
+  const float* pcb = a.pc + (int64_t)b * 128;
+  for (int base_it = 0; base_it < n_items; base_it += 2 * NT) {
+    int kind[2], hq[2], ii[2], r[2], lr[2], c0[2], ns[2], sl0[2];
+    bool have[2];
+    float2 pcs[2][kMaxPieces], cs[2], bs[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = base_it + u * NT + ctid;
+      have[u] = it < n_items;
+      const int itc = have[u] ? it : 0;
+      if (itc < a.group * half) {
+        kind[u] = 0;
+        hq[u] = itc / half;
+        ii[u] = itc - hq[u] * half;
+        const int j = g * a.group + hq[u];
+        r[u] = j / nq;
+        lr[u] = (j - r[u] * nq) * D + 2 * ii[u];
+      } else {
+        kind[u] = itc < (a.group + 1) * half ? 1 : 2;
+        hq[u] = 0;
+        ii[u] = itc - (a.group + kind[u] - 1) * half;
+        r[u] = kv_rank;
+        lr[u] = (nq + (kind[u] == 2 ? kvr : 0) + kv_local) * D + 2 * ii[u];
+      }
+      const int ts = r[u] * a.pc_a_tiles + lr[u] / 128;
+      c0[u] = ((ts * K + 1) * Gp - 1) / T;                       // owner of the tile's first step
+      ns[u] = (((ts + 1) * K) * Gp - 1) / T - c0[u] + 1;          // pieces of the tile
+      sl0[u] = (c0[u] * T) / Gp == ts * K ? 0 : 1;                // slot of the first piece
+      const float* src = pcb + lr[u] % 128;
+#pragma unroll
+      for (int q = 0; q < kMaxPieces; ++q)
+        pcs[u][q] = have[u] && q < ns[u]
+                        ? __ldcg(reinterpret_cast<const float2*>(
+                              src + ((int64_t)(c0[u] + q) * 2 + (q == 0 ? sl0[u] : 0)) * piece))
+                        : make_float2(0.f, 0.f);
+      cs[u] = (have[u] && kind[u] != 2 && pos_ok) ? __ldg(a.rope + (int64_t)pos * half + ii[u])
+                                                  : make_float2(1.f, 0.f);
+      bs[u] = make_float2(0.f, 0.f);
+      if (have[u] && a.qkv_bias) {
+        const uint16_t* bb = a.qkv_bias + (int64_t)r[u] * a.nqkv_r + lr[u];
+        bs[u] = make_float2(bf16_to_f(bb[0]), bf16_to_f(bb[1]));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!have[u]) continue;
+      float2 x = pcs[u][0];
+#pragma unroll
+      for (int q = 1; q < kMaxPieces; ++q)
+        if (q < ns[u]) { x.x += pcs[u][q].x; x.y += pcs[u][q].y; }
+      // a tile cut in more pieces than were loaded together (small grids)
+      const float* src = pcb + lr[u] % 128;
+      for (int q = kMaxPieces; q < ns[u]; ++q) {
+        const float2 p2 = __ldcg(reinterpret_cast<const float2*>(src + (int64_t)(c0[u] + q) * 2 * piece));
+        x.x += p2.x;
+        x.y += p2.y;
+      }
+      x.x = x.x * rs + bs[u].x;
+      x.y = x.y * rs + bs[u].y;
+      const int i = ii[u];
+      if (kind[u] == 2) {
+        // V rows in natural order: features 2i and 2i + 1
+        const uint16_t v0 = f_to_bf16(x.x), v1 = f_to_bf16(x.y);
+        vnew[2 * i] = bf16_to_f(v0);
+        vnew[2 * i + 1] = bf16_to_f(v1);
+        if (write && pos_ok) {
+          uint16_t* dst = a.v_cache + (int64_t)(g / kvr) * a.kv_copy_stride +
+                          (((int64_t)b * kvr + kv_local) * a.l_max + pos) * D;
+          *reinterpret_cast<uint32_t*>(dst + 2 * i) = (uint32_t)v0 | ((uint32_t)v1 << 16);
+        }
+        continue;
+      }
+      const uint16_t y1 = f_to_bf16(x.x * cs[u].x - x.y * cs[u].y);  // feature i
+      const uint16_t y2 = f_to_bf16(x.y * cs[u].x + x.x * cs[u].y);  // feature i + d/2
+      if (kind[u] == 0) {
+        uint16_t* qr = reinterpret_cast<uint16_t*>(sQ + hq[u] * qrow_bytes);
+        qr[i] = y1;
+        qr[i + half] = y2;
+      } else {
+        knew[i] = bf16_to_f(y1);
+        knew[i + half] = bf16_to_f(y2);
+        if (write && pos_ok) {
+          uint16_t* dst = a.k_cache + (int64_t)(g / kvr) * a.kv_copy_stride +
+                          (((int64_t)b * kvr + kv_local) * a.l_max + pos) * D;
+          dst[i] = y1;
+          dst[i + half] = y2;
+        }
+      }
+    }
+  }
+}
+
+// Score of the new key against query row `row` (log2 units): the row's 16
+// threads (one half-warp) each take features cl, cl + 16, ... and combine.
+template <int D>
+__device__ __forceinline__ float new_key_score(const uint8_t* sQ, int qrow_bytes, const float* knew,
+                                               int row, int cl, float scale_log2) {
+  const uint16_t* qr = reinterpret_cast<const uint16_t*>(sQ + row * qrow_bytes);
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < D / 16; ++j) s = fmaf(bf16_to_f(qr[cl + 16 * j]), knew[cl + 16 * j], s);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s * scale_log2;
+}
+
+
 template <int D>
 __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   using L = DecSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* tiles = smem;
-  uint8_t* sQ = tiles + L::kStages * L::kStageBytes;
-  float* comb = reinterpret_cast<float*>(sQ + 16 * L::kQRow);
-  uint64_t* full = reinterpret_cast<uint64_t*>(comb + L::kComb);
-  uint64_t* empty = full + L::kStages;
-  int* last_flag = reinterpret_cast<int*>(empty + L::kStages);
+  const typename L::Layout LY = L::layout(a.stages, a.group);
+  uint8_t* tiles = smem + LY.tiles;
+  uint8_t* sQ = smem + LY.sq;
+  float* comb = reinterpret_cast<float*>(smem + LY.comb);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY.bars);
+  uint64_t* empty = full + L::kMaxStages;
+  int* last_flag = reinterpret_cast<int*>(smem + LY.misc);
+  float* red = reinterpret_cast<float*>(smem + LY.misc + 16);  // 8 floats
+  float* knew = reinterpret_cast<float*>(smem + LY.knew);       // [D]
+  float* vnew = knew + D;                                        // [D]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = L::kStages;
+  const int S = a.stages;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kDecGroupWarps); }
     fence_barrier_init();
@@ -135,7 +343,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       // has completed.  Tiles wholly below the position therefore fill the
       // first stages before the wait for q and the new rows.
       int64_t u = beg;
-      while (u < end && n < (uint32_t)S && (tile + 1) * kKeyTile <= a.positions[b]) {
+      while (u < end && n < (uint32_t)S &&
+             (a.qkv_pieces || (tile + 1) * kKeyTile <= a.positions[b])) {
         issue(n);
         ++n;
         if (++u < end) advance();
@@ -154,8 +363,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       pdl_wait();
     }
   } else {
-    pdl_wait();  // q and the newest cache rows were written by the preceding kernels
     const int ctid = threadIdx.x;  // 0..255
+    // The first segment's position and, with the deferred qkv, its token's
+    // 1/rms: they read only the batch and the hidden state, which every kernel
+    // before the qkv GEMM has finished writing when this kernel starts (the
+    // GEMM signals its dependents after its own wait), so they overlap the
+    // GEMM's end.
+    int first_pos = 0;
+    float first_rs = 1.f;
+    if (beg < end) {
+      const int b0 = static_cast<int>((beg / TB) / a.n_kv);
+      first_pos = a.positions[b0];
+      if (a.qkv_pieces) first_rs = token_rs<D>(a, b0, red);
+    }
+    pdl_wait();  // q and the newest cache rows were written by the preceding kernels
     uint32_t n_base = 0;           // CTA-local index of the segment's first unit
     bool alive = true;
     for (int64_t u0 = beg; u0 < end;) {
@@ -164,17 +385,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       const int len = static_cast<int>(seg_end - u0);
       const int tile0 = static_cast<int>(u0 - bg * TB);
       const int b = static_cast<int>(bg / a.n_kv), g = static_cast<int>(bg % a.n_kv);
-      const int pos = a.positions[b];
+      const bool first_seg = u0 == beg;
+      const int pos = first_seg ? first_pos : a.positions[b];
       // stage the group's query rows (16 rows, zero beyond the group)
       for (int i = ctid; i < 16 * (D / 8); i += kDecWarps * 32) {
         const int row = i / (D / 8), ch = i % (D / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < a.group)
+        if (row < a.group && !a.qkv_pieces)
           v = *reinterpret_cast<const uint4*>(a.q + (int64_t)b * a.ld_q +
                                               (int64_t)(g * a.group + row) * D + ch * 8);
         *reinterpret_cast<uint4*>(sQ + row * L::kQRow + ch * 16) = v;
       }
       bar_sync(1, kDecWarps * 32);
+      if (a.qkv_pieces) {
+        // q, and the new token's k and v, from the qkv GEMM's pieces; the
+        // pair's first CTA stores the new K/V row in the cache
+        const bool writer = owner_of(bg * TB, T, G) == c;
+        const float rs = first_seg ? first_rs : token_rs<D>(a, b, red);
+        qkv_from_pieces<D>(a, b, g, pos, rs, writer, sQ, L::kQRow, knew, vnew);
+        bar_sync(1, kDecWarps * 32);
+      }
       uint32_t qa[D / 16][4];
       load_q_frags<D>(smem_u32(sQ), L::kQRow, qa);
       float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -183,7 +413,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       for (int nt = 0; nt < D / 8; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
-      const int lim[2] = {pos, pos};
+      // with the deferred qkv the new key is merged at the end, not read from the cache
+      const int last_key = a.qkv_pieces ? pos - 1 : pos;
+      const int lim[2] = {last_key, last_key};
       // group grp takes tiles grp, grp + 2, ... of the segment; every warp of
       // it takes its own 16 keys of the tile, so a stage is released after a
       // quarter of that tile's work and the other stages keep streaming
@@ -197,7 +429,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) { alive = false; break; }
         const int key0 = (tile0 + i) * kKeyTile + wq * kWarpKeys;
-        if (key0 <= pos) {
+        if (key0 <= last_key) {
           const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
           attn_tile<D, kWarpKeys / 8>(qa, st, st + L::kTileBytes, wq * kWarpKeys, key0, lim,
                                       a.scale_log2, m, l, o);
@@ -212,33 +444,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
       }
       // combine: every warp's (m, l, O) meets the others in smem
+      // (only the KV head's query rows: rows >= group hold no query)
       constexpr int CL = L::kCombLd;
-      float* cw = comb + warp * 16 * CL;
+      const int GR = a.group;
+      float* cw = comb + warp * GR * CL;
       const int r0 = lane >> 2;
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt) {
-        const int col = nt * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(cw + r0 * CL + col) = make_float2(o[nt][0], o[nt][1]);
-        *reinterpret_cast<float2*>(cw + (r0 + 8) * CL + col) = make_float2(o[nt][2], o[nt][3]);
-      }
-      if ((lane & 3) == 0) {
-        cw[r0 * CL + D] = m[0]; cw[r0 * CL + D + 1] = l[0];
-        cw[(r0 + 8) * CL + D] = m[1]; cw[(r0 + 8) * CL + D + 1] = l[1];
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = r0 + hh * 8;
+        if (r >= GR) continue;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          const int col = nt * 8 + (lane & 3) * 2;
+          *reinterpret_cast<float2*>(cw + r * CL + col) = make_float2(o[nt][hh * 2], o[nt][hh * 2 + 1]);
+        }
+        if ((lane & 3) == 0) { cw[r * CL + D] = m[hh]; cw[r * CL + D + 1] = l[hh]; }
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
       // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128): columns
       // cl, cl + 16, ... so that a row's 16 threads read 16 consecutive floats
       constexpr int CPT = D / 16;
       const int row = ctid >> 4, cl = ctid & 15;
+      const float s_new =
+          a.qkv_pieces ? new_key_score<D>(sQ, L::kQRow, knew, row, cl, a.scale_log2) : -INFINITY;
+      const int crow = row < GR ? row : 0;  // rows >= group: computed, never stored
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * 16 + row) * CL + D]);
+      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * GR + crow) * CL + D]);
       float ll = 0.f, acc[CPT];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
 #pragma unroll 2
       for (int w = 0; w < kDecWarps; ++w) {
-        const float* cr = comb + (w * 16 + row) * CL;
+        const float* cr = comb + (w * GR + crow) * CL;
         const float mw = cr[D];
         if (mw == -INFINITY) continue;
         const float sc = exp2f(mw - mm);
@@ -248,7 +486,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       }
       const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
       uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
+      // the new key's state (score s_new, weight 1, value vnew) joins the
+      // pair's final combination
+      auto add_new_key = [&](float& m_, float& l_, float (&o_)[CPT]) {
+        const float mn = fmaxf(m_, s_new);
+        const float so = m_ == -INFINITY ? 0.f : exp2f(m_ - mn);
+        const float sn = exp2f(s_new - mn);
+        l_ = l_ * so + sn;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) o_[j] = o_[j] * so + vnew[cl + 16 * j] * sn;
+        m_ = mn;
+      };
       if (nseg == 1) {
+        if (a.qkv_pieces) add_new_key(mm, ll, acc);
         if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
       } else {
         const int first_c = owner_of(bg * TB, T, G);
@@ -287,6 +537,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + cl + 16 * j]) * sc;
           }
+          if (a.qkv_pieces) add_new_key(M2, L2, acc2);
           if (row < a.group) store_out_row<CPT>(orow, acc2, 1.f / L2);
           if (ctid == 0) a.tickets[bg] = 0;
         }
@@ -436,15 +687,24 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
 // ============================================================================
 template <int D>
 static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
-  const size_t smem = DecSmem<D>::bytes(0);
+  const size_t smem = DecSmem<D>::bytes(a.stages, a.group);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   return launch_k(attn_decode_kernel<D>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
+}
+
+// The most K/V stages (even, at most DecSmem::kMaxStages) whose shared memory
+// fits next to the combine buffer of `rows` query rows per KV head.
+template <int D>
+static int decode_stages_t(int rows) {
+  for (int s = DecSmem<D>::kMaxStages; s >= 2; s -= 2)
+    if (DecSmem<D>::bytes(s, rows) <= 227 * 1024) return s;
+  return 0;
 }
 
 template <int D>
@@ -471,10 +731,9 @@ cudaError_t launch_attn_prefill(const AttnArgs& a, int n_qb, cudaStream_t st) {
 
 size_t attn_decode_partial_floats(int head_dim) { return 16 * (size_t)(head_dim + 2); }
 
+int attn_decode_stages(int head_dim, int rows) {
+  return head_dim == 128 ? decode_stages_t<128>(rows) : decode_stages_t<64>(rows);
+}
+
 }  // namespace tpk
 
-namespace tpk {
-size_t attn_decode_smem_bytes(int head_dim) {
-  return head_dim == 128 ? DecSmem<128>::bytes(0) : DecSmem<64>::bytes(0);
-}
-}  // namespace tpk

@@ -34,6 +34,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rms.cuh"
 
 namespace tpk {
 
@@ -557,7 +558,8 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
   // projection is the exception that signals late (after its wait): decode
   // attention reads the cache rows of earlier steps before its own wait, which
   // is sound only if every kernel before this one has completed.
-  if constexpr (EPI != EPI_QKV) pdl_launch_dependents();
+  constexpr bool kLateSignal = EPI == EPI_QKV || EPI == EPI_QKV_PIECES;
+  if constexpr (!kLateSignal) pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
     }
   } else {
     pdl_wait();
-    if constexpr (EPI == EPI_QKV) pdl_launch_dependents();
+    if constexpr (kLateSignal) pdl_launch_dependents();
     // Epilogue warp w reads TMEM lanes of quadrant w % 4 (its 32 rows); in the
     // decode orientation two warps share a quadrant and take alternate
     // U-column units of every 16-column span.
@@ -720,31 +722,9 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
         // the folded RMSNorm's 1/rms of every token, one warp per token, while
         // the MMA warp streams the weights (the hidden rows come from L2)
         float* rs = reinterpret_cast<float*>(tok + 4 * kSwapMaxTokens);
-        const int ew = et >> 5, nv = a.e.norm_width >> 3;
+        const int ew = et >> 5;
         for (int m = ew; m < a.e.M; m += kEpiWarps<SWAP>) {
-          const uint4* xr = reinterpret_cast<const uint4*>(a.e.norm_src + (int64_t)m * a.e.norm_ld);
-          float ss = 0.f;
-          auto add_sq = [&](const uint4& p) {
-            const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
-              ss = fmaf(lo, lo, ss);
-              ss = fmaf(hi, hi, ss);
-            }
-          };
-          // eight independent 16-byte loads in flight per lane, then their squares
-          int v = lane;
-          for (; v + 7 * 32 < nv; v += 8 * 32) {
-            uint4 p[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) p[q] = __ldcg(xr + v + q * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) add_sq(p[q]);
-          }
-          for (; v < nv; v += 32) add_sq(__ldcg(xr + v));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          const float ss = warp_row_sumsq(a.e.norm_src + (int64_t)m * a.e.norm_ld, a.e.norm_width);
           if (lane == 0) rs[m] = 1.0f / sqrtf(ss / (float)a.e.norm_width + a.e.norm_eps);
         }
         if (et >= a.e.M && et < kSwapMaxTokens) rs[et] = 0.f;
@@ -798,6 +778,26 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < kUnit<SWAP>; ++j) red[(c0 + j) * 128 + row] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        ++seg;
+        continue;
+      }
+      if constexpr (EPI == EPI_QKV_PIECES) {
+        // slot 0: the segment where this CTA's range starts, slot 1: the next
+        // (a range never spans more than two tiles: the host keeps the grid at
+        // least as large as the tile count)
+        const int64_t ts = sg.tile - dp_tiles;
+        const int my_slot = (beg / K == ts) ? 0 : 1;
+        float* mine = a.partials + ((int64_t)(c * 2 + my_slot) * BN) * 128;
+        for (int c0 = half * U; c0 < BN; c0 += NH * U) {
+          float v[16];
+          tld(taddr + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < kUnit<SWAP>; ++j) mine[(c0 + j) * 128 + row] = v[j];
         }
         tc_fence_before();
         __syncwarp();

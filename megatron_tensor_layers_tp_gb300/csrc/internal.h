@@ -21,6 +21,9 @@ enum Epi : int {
   EPI_LOGITS = 5,   // LM head: logits placed in the rank's vocab slot
   EPI_RESID_SQ = 6, // EPI_RESID (decode orientation) that also leaves the next
                     // RMSNorm's sums of squares (EpiArgs::sq_out)
+  EPI_QKV_PIECES = 7,  // qkv in the decode orientation, stream-K: every CTA only
+                       // stores its fp32 pieces; the decode attention kernel sums
+                       // them and finishes the qkv epilogue (norm, bias, RoPE, cache)
 };
 
 struct EpiArgs {
@@ -119,9 +122,34 @@ struct AttnArgs {
   int tiles_per_bg;
   int64_t total_units;
   int grid;
+  int stages;                 // K/V stages in shared memory (even)
   float* partials;            // [grid][2][16][d+2]
   int* tickets;               // [n_seqs*n_kv]
   int* status;
+  // decode, qkv reduction deferred to this kernel (the qkv GEMM ran with
+  // EPI_QKV_PIECES): each CTA sums the GEMM's fp32 pieces of its sequence's q,
+  // k and v rows in K order, scales them by the token's 1/rms, adds the bias,
+  // applies RoPE, writes the new K/V cache row and merges the new key into the
+  // softmax itself; cached keys at the new position are not read
+  int qkv_pieces;
+  const float* pc;            // pieces [pc_grid][2][pc_bn][128] fp32 (stream-K slots)
+  int64_t pc_total;           // the GEMM's stream-K K steps
+  int pc_grid, pc_k, pc_bn;   // its grid, K steps per tile, token tile width
+  int pc_a_tiles;             // 128-row tiles per rank
+  int nqkv_r;                 // qkv shard rows per rank
+  int q_per_rank, kv_replicas;
+  const uint16_t* qkv_bias;   // [ranks][nqkv_r] or null
+  const float2* rope;         // [max_positions][d/2]
+  uint16_t* k_cache;          // [copies][n_seqs][kv_r][l_max][d]
+  uint16_t* v_cache;
+  int64_t kv_copy_stride;
+  int norm_mode;              // 1/rms of the token as EpiArgs: 0 none, 1 rows, 2 partial sums
+  const uint16_t* norm_src;
+  int64_t norm_ld;
+  int norm_width;
+  float norm_eps;
+  const float* norm_partials;
+  int norm_slots;
 };
 
 // Every kernel on the forward path is launched with programmatic stream
@@ -170,12 +198,14 @@ TPK_DECLARE_EPI(3)
 TPK_DECLARE_EPI(4)
 TPK_DECLARE_EPI(5)
 TPK_DECLARE_EPI(6)
+TPK_DECLARE_EPI(7)
 
 // attention.cu
 cudaError_t launch_attn_decode(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_prefill(const AttnArgs& a, int n_qb, cudaStream_t st);
 size_t attn_decode_partial_floats(int head_dim);
-size_t attn_decode_smem_bytes(int head_dim);
+// the decode kernel's K/V stage count for `rows` query rows per KV head
+int attn_decode_stages(int head_dim, int rows);
 
 // small.cu
 cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,

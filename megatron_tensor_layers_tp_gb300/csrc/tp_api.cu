@@ -517,6 +517,7 @@ int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem) {
     case 4: n = gemm_max_clusters_epi4(swap, cluster_x, smem); break;
     case 5: n = gemm_max_clusters_epi5(swap, cluster_x, smem); break;
     case 6: n = gemm_max_clusters_epi6(swap, cluster_x, smem); break;
+    case 7: n = gemm_max_clusters_epi7(swap, cluster_x, smem); break;
   }
   cache.push_back({key, n});
   return n;
@@ -531,6 +532,7 @@ cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cuda
     case 4: return launch_gemm_epi4(swap, a, smem, st);
     case 5: return launch_gemm_epi5(swap, a, smem, st);
     case 6: return launch_gemm_epi6(swap, a, smem, st);
+    case 7: return launch_gemm_epi7(swap, a, smem, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -1023,6 +1025,8 @@ static tp_status prep_attention(const tp_model* m, const tp_batch_t* b, uint16_t
       }
     }
     a.grid = grid;
+    a.stages = attn_decode_stages(d, a.group);
+    if (a.stages < 2) return TP_ERR_UNSUPPORTED;
     a.partials = at<float>(ws, L.attn_partials);
     a.tickets = at<int>(ws, L.attn_tickets);
   }
@@ -1100,11 +1104,57 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   // qkv (column-parallel) + RoPE + K/V into the rank caches
   EpiArgs e = qkv_epi(m, b, M, q, kc, vc);
   if ((s = norm_in(e, *h_sq, &xin)) != TP_OK) return s;
-  if ((s = run_column(m, "gemm_qkv", Ls.qkv_folded, xin, H, M, EPI_QKV, e, ws, L, st)) != TP_OK)
-    return s;
-  // attention
   AttnArgs a;
   if ((s = prep_attention(m, b, kc, vc, q, o, ws, L, m->num_sms, a)) != TP_OK) return s;
+  if (b->mode == TP_DECODE && swap) {
+    // Decode: the qkv GEMM only leaves its stream-K pieces (no arrival
+    // tickets, no fix-up at its end); each attention CTA sums the pieces of
+    // its own sequence and KV head and finishes the qkv epilogue (norm, bias,
+    // RoPE, new K/V cache row) while its cache tiles stream in.
+    GemmArgs g;
+    GemmPlan p;
+    if ((s = prep_column(m, Ls.qkv_folded, xin, H, M, EPI_QKV_PIECES, e, ws, L, g, p)) != TP_OK)
+      return s;
+    const int64_t n_tiles = (int64_t)g.n_groups * g.a_tiles * g.b_tiles;
+    g.cluster_split = 1;
+    g.dp_waves = 0;
+    g.sk_ctas = 0;
+    g.total_iters = n_tiles * g.k_slices * g.k_iters_slice;
+    g.grid = (int)std::min<int64_t>(m->num_sms, g.total_iters);
+    // every CTA's range spans at most two tiles when there are no more tiles
+    // than CTAs; the attention kernel locates pieces in 32-bit arithmetic
+    if (n_tiles <= g.grid && g.total_iters * g.grid < (int64_t)1 << 31) {
+      TP_CHECK_CUDA(launch(m, "gemm_qkv", st, [&] {
+        return launch_gemm(true, EPI_QKV_PIECES, g, p.smem, st);
+      }));
+      a.qkv_pieces = 1;
+      a.pc = g.partials;
+      a.pc_total = g.total_iters;
+      a.pc_grid = g.grid;
+      a.pc_k = g.k_slices * g.k_iters_slice;
+      a.pc_bn = g.BN;
+      a.pc_a_tiles = g.a_tiles;
+      a.nqkv_r = Ls.qkv_folded.rows;
+      a.q_per_rank = c.q_heads_per_rank;
+      a.kv_replicas = c.kv_replicas;
+      a.qkv_bias = Ls.qkv_folded.bias;
+      a.rope = m->rope;
+      a.k_cache = kc;
+      a.v_cache = vc;
+      a.kv_copy_stride = e.kv_copy_stride;
+      a.norm_mode = e.norm_mode;
+      a.norm_src = e.norm_src;
+      a.norm_ld = e.norm_ld;
+      a.norm_width = e.norm_width;
+      a.norm_eps = e.norm_eps;
+      a.norm_partials = e.norm_partials;
+      a.norm_slots = e.norm_slots;
+    }
+  }
+  if (!a.qkv_pieces &&
+      (s = run_column(m, "gemm_qkv", Ls.qkv_folded, xin, H, M, EPI_QKV, e, ws, L, st)) != TP_OK)
+    return s;
+  // attention
   if (b->mode == TP_DECODE) {
     TP_CHECK_CUDA(launch(m, "attn_decode", st, [&] { return launch_attn_decode(a, st); }));
   } else {
