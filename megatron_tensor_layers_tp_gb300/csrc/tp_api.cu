@@ -191,7 +191,11 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
   a.cluster_split = 1;
-  if (p.swap) {
+  // Up to 16 tokens the pieces are small (8 KB per 128-row tile) and
+  // stream-K over every SM wins (measured, same box, alternating runs:
+  // Llama-8B decode layer 111.5 -> 110.7 us); at 64 tokens the cluster split
+  // does (Qwen-32B layer 279.5 vs 285.3 us).
+  if (p.swap && p.BN > 16) {
     // the largest cluster (8 CTAs at most, portable) whose tiles x s CTAs fill
     // at least 65% of the SMs in one wave (measured: a cluster split beats
     // stream-K's fix-up from there on); the occupancy query decides whether

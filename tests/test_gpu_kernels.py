@@ -238,8 +238,9 @@ def test_prefill_orientation_schedules_match_oracle(M, inter, t):
 def test_decode_cluster_split_matches_oracle(t, M, hidden, n_heads):
     # hidden 4096: 32 row-parallel output tiles (clusters of 4) and 48 qkv
     # tiles; hidden 5120: 40 row-parallel tiles (clusters of 3) and 56 qkv
-    # tiles (clusters of 2) -- the decode schedule splits them over clusters
-    # of CTAs whose K pieces are summed on chip
+    # tiles (clusters of 2) -- above 16 tokens the decode schedule splits
+    # them over clusters of CTAs whose K pieces are summed on chip; up to 16
+    # tokens it runs stream-K over every SM
     w = _wl(hidden=hidden, n_heads=n_heads, n_kv=8, head_dim=128, inter=2048)
     m, _, _ = _model(w, t, head=False)
     W = oracle_layer(w, 0)
