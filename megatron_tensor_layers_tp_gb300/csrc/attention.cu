@@ -507,15 +507,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
         for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + cl + 16 * j] = acc[j];
         if ((ctid & 15) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
-        __threadfence();
+        // publish the record and take the pair's ticket: one thread fences
+        // for the CTA around the increment (the barriers carry the ordering)
         bar_sync(1, kDecWarps * 32);
         if (ctid == 0) {
+          fence_acq_rel_gpu();
           const int old = atomicAdd(&a.tickets[bg], 1);
+          fence_acq_rel_gpu();
           *last_flag = (old == nseg - 1) ? 1 : 0;
         }
         bar_sync(1, kDecWarps * 32);
         if (*last_flag) {
-          __threadfence();
           float M2 = -INFINITY;
           for (int sgi = 0; sgi < nseg; ++sgi) {
             const int cc = first_c + sgi;

@@ -854,15 +854,21 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        __threadfence();
+        // Publish the piece and take the tile's ticket: the named barrier
+        // orders every epilogue thread's stores before one thread's GPU-scope
+        // fence and ticket increment; a second fence after the increment, and
+        // the barrier after it, order the last arriver's reads of the other
+        // pieces after the others' increments (one fence pair per piece
+        // instead of a fence per thread)
         bar_sync(1, ET);
         if (threadIdx.x == 64) {
+          fence_acq_rel_gpu();
           const int old = atomicAdd(&a.tickets[sg.tile], 1);
+          fence_acq_rel_gpu();
           *last_flag = (old == nseg - 1) ? 1 : 0;
         }
         bar_sync(1, ET);
         if (*last_flag) {
-          __threadfence();
           // The pieces in K order are those of CTAs c_first, c_first + 1, ...;
           // only the first can have started its range before this tile (its
           // piece then sits in slot 1).  Loads of up to 4 pieces are in flight
