@@ -51,6 +51,10 @@ def parse():
     p.add_argument("--configs", type=int, default=1)
     p.add_argument("--prefill-only", type=int, default=0,
                    help="profiling aid: run only the prefill section and print its JSON")
+    p.add_argument("--prefill-bn", type=int, default=0,
+                   help="prefill GEMMs' output-feature tile width (0: chosen per GEMM)")
+    p.add_argument("--prefill-pairs", type=int, default=0,
+                   help="prefill GEMMs on CTA pairs: 0 auto, 1 always, 2 never")
     p.add_argument("--cpu-budget-s", type=float, default=15.0)
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     return p.parse_args()
@@ -514,7 +518,8 @@ def run_ours(args, rank, world):
         model.close()
         torch.cuda.empty_cache()
     if args.prefill and rank == 0 and world == 1:
-        prefill, prefill_detail = prefill_section(stream)
+        prefill, prefill_detail = prefill_section(stream, prefill_bn=args.prefill_bn,
+                                                   prefill_pairs=args.prefill_pairs)
     if args.configs and rank == 0 and world == 1:
         for name in ("qwen32b_decode", "qwen32b_decode_kv4"):
             configs[name], configs_detail[name] = decode_layer_section(name, stream, hbm_peak)
@@ -665,7 +670,7 @@ def full_forward_section(stream, hbm_peak, reps=10, warmup=3):
     return compact, detail
 
 
-def prefill_section(stream, reps=10):
+def prefill_section(stream, reps=10, prefill_bn=0, prefill_pairs=0):
     """Llama-3.1-8B-shaped prefill chunk at t = 4: 8 sequences x 256 tokens
     through the vocab-parallel embedding, one decoder layer and the
     vocab-parallel LM head on each sequence's last token.  Reports every
@@ -696,7 +701,8 @@ def prefill_section(stream, reps=10):
         synth.fill_normal_(lm, w.seed, synth.tensor_id("lm_head"), w.sigma_w)
         fn = torch.ones(H, dtype=torch.bfloat16, device="cuda")
         cfg = make_config(H, w.n_heads, w.n_kv_heads, d, I, V, 1, t, w.rms_eps, w.rope_theta,
-                          max_positions=w.l_max)
+                          max_positions=w.l_max, prefill_bn=prefill_bn,
+                          prefill_cta_pairs=prefill_pairs)
         model = TPModel(cfg, [L], emb, fn, lm, max_tokens=M, stream=stream)
         del L, emb, lm
         k = model.alloc_kv(w.n_seqs, w.l_max)
@@ -850,7 +856,8 @@ def main():
     if args.prefill_only:
         import torch
         stream = torch.cuda.Stream()
-        print(json.dumps({"prefill": prefill_section(stream)[1]}), flush=True)
+        print(json.dumps({"prefill": prefill_section(stream, prefill_bn=args.prefill_bn,
+                                                   prefill_pairs=args.prefill_pairs)[1]}), flush=True)
         return
     if world > 1:
         import torch

@@ -98,6 +98,17 @@ typedef struct {
                             copy engine), 1 = always cudaMemcpyAsync */
   int32_t plain_column_shards; /* 1: keep an unfolded copy of every qkv / gate_up
                             shard for tp_column_linear (see tp_load_shards) */
+  int32_t prefill_bn;    /* output-feature tile width of the GEMMs above 64
+                            tokens: 0 = chosen per GEMM (the width among 256,
+                            224, 192, 160, 128 whose whole-tile waves over the
+                            SMs take least time, 256 when that GEMM has fewer
+                            tiles than SMs); else one of those five, used by
+                            every such GEMM (any other value: TP_ERR_ARG) */
+  int32_t prefill_cta_pairs; /* GEMMs above 64 tokens on pairs of SMs
+                            (tcgen05 cta_group::2, 256 token rows per tile):
+                            0 = when the GEMM has at least one wave of such
+                            tiles, 1 = always, 2 = never (single-CTA kernel);
+                            any other value: TP_ERR_ARG */
   /* derived, written by tp_config */
   int32_t vocab_padded;
   int32_t vocab_per_rank;

@@ -27,7 +27,8 @@ class tp_config_t(Structure):
     _fields_ = [(n, c_int32) for n in ("hidden", "n_heads", "n_kv_heads", "head_dim", "intermediate",
                                        "vocab", "n_layers", "t")] + \
                [("rms_eps", c_float), ("rope_theta", c_float), ("max_positions", c_int32),
-                ("attn_dp", c_int32), ("host_io", c_int32), ("plain_column_shards", c_int32)] + \
+                ("attn_dp", c_int32), ("host_io", c_int32), ("plain_column_shards", c_int32),
+                ("prefill_bn", c_int32), ("prefill_cta_pairs", c_int32)] + \
                [(n, c_int32) for n in ("vocab_padded", "vocab_per_rank", "q_heads_per_rank",
                                        "kv_heads_per_rank", "kv_replicas", "kv_copies",
                                        "inter_per_rank", "attn_tp")]

@@ -98,6 +98,8 @@ struct GemmArgs {
   int dp_waves;             // W: tiles [0, W*G) are whole-tile, data-parallel
   int cluster_split;        // s > 1: cluster of s CTAs per tile, K split s ways (DSMEM sum)
   int64_t total_iters;      // (n_tiles - W*G) * k_slices * k_iters_slice (stream-K part)
+  int pair;                 // 1: prefill orientation on CTA pairs (gemm_pair_kernel): a_tiles
+                            // counts 256-row tiles, tmB has a box of BN/2 rows, grid = 2 x pairs
   int sk_ctas;              // CTAs 0..sk_ctas-1 share the stream-K part (0: all G); with
                             // sk_ctas = n_tiles - W*G each of them takes one whole tile
   float* partials;          // [G][2][BN][128]
@@ -187,10 +189,12 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 
 // gemm.cu / gemm_epi*.cu
 cudaError_t launch_gemm(bool swap, int epi, const GemmArgs& a, size_t smem, cudaStream_t st);
-int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem);
+// co-resident clusters of cluster_x CTAs of the GEMM kernel (pair: the CTA-pair
+// kernel, cluster_x = 2) with `smem` bytes each
+int gemm_max_clusters(bool swap, bool pair, int epi, int cluster_x, size_t smem);
 #define TPK_DECLARE_EPI(E)                                                                   \
   cudaError_t launch_gemm_epi##E(bool swap, const GemmArgs& a, size_t smem, cudaStream_t st); \
-  int gemm_max_clusters_epi##E(bool swap, int cluster_x, size_t smem);
+  int gemm_max_clusters_epi##E(bool swap, bool pair, int cluster_x, size_t smem);
 TPK_DECLARE_EPI(0)
 TPK_DECLARE_EPI(1)
 TPK_DECLARE_EPI(2)

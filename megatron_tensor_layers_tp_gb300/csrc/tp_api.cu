@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -16,13 +17,19 @@
 
 using namespace tpk;
 
+// Output-feature tile widths of the prefill orientation, widest first.
+constexpr int kPrefillBNs[] = {256, 224, 192, 160, 128};
+constexpr int kNumPrefillBN = 5;
+constexpr int kPrefillBN = kPrefillBNs[0];
+
 struct ShardedLinear {
   uint16_t* data = nullptr;  // [t][rows][cols]
   uint16_t* bias = nullptr;  // optional: [ranks][rows] (column-parallel) or [rows] (row-parallel)
   int rows = 0, cols = 0;    // per rank
   int ranks = 0;             // t, or attn_tp for the attention block
   CUtensorMap tm_a;          // box (64, 128, 1): weight on the MMA M side (decode)
-  CUtensorMap tm_b;          // box (64, 256, 1): weight on the MMA N side (prefill)
+  CUtensorMap tm_b[kNumPrefillBN];  // box (64, kPrefillBNs[i], 1): weight on the MMA N side (prefill)
+  CUtensorMap tm_h[kNumPrefillBN];  // box (64, kPrefillBNs[i] / 2, 1): one CTA's half (CTA pairs)
 };
 
 struct LayerShards {
@@ -59,7 +66,6 @@ struct tp_model {
 
 namespace {
 
-constexpr int kPrefillBN = 256;
 constexpr int kAttnWholeMaxTiles = 128;  // decode attention: whole pairs up to this many key tiles per CTA
 constexpr int kNormInGemmTokens = 32;  // folded RMSNorm applied inside the GEMM up to here
 constexpr size_t kAlign = 256;
@@ -159,15 +165,24 @@ tp_status dev_alloc(tp_model* m, T** p, size_t bytes) {
 // ---------------------------------------------------------------- planning
 struct GemmPlan {
   bool swap;
+  bool pair;  // prefill orientation on CTA pairs
   int BN, stages, tmem_cols;
   size_t smem;
 };
 
-GemmPlan plan_gemm(int M) {
+int prefill_bn_index(int bn) {
+  for (int i = 0; i < kNumPrefillBN; ++i)
+    if (kPrefillBNs[i] == bn) return i;
+  return -1;
+}
+
+GemmPlan plan_gemm(int M, int bn = kPrefillBN, bool pair = false) {
   GemmPlan p;
   p.swap = M <= kSwapMaxTokens;
-  p.BN = p.swap ? std::max(16, cdiv(M, 16) * 16) : kPrefillBN;
-  const int stage = 128 * 128 + p.BN * 128;
+  p.pair = !p.swap && pair;
+  p.BN = p.swap ? std::max(16, cdiv(M, 16) * 16) : bn;
+  // one CTA's stage: 128 rows of A and its rows of B (half of them on a pair)
+  const int stage = 128 * 128 + (p.pair ? p.BN / 2 : p.BN) * 128;
   const int budget = 200 * 1024;
   p.stages = std::min(8, budget / stage);
   int cols = 32;
@@ -175,6 +190,54 @@ GemmPlan plan_gemm(int M) {
   p.tmem_cols = cols;
   p.smem = 1024 + (size_t)p.stages * stage + (2 * p.stages + 5) * 8 + 16 + 5 * kSwapMaxTokens * 4;
   return p;
+}
+
+// Prefill orientation: whether a GEMM runs on CTA pairs, and its
+// output-feature tile width.
+//  - CTA pairs (tcgen05 cta_group::2, tiles of 256 token rows) when the GEMM
+//    has at least one whole wave of pair tiles at width 256: per SM they move
+//    a third less operand data per K step than a single CTA's 128 x 256 tile,
+//    and the single-CTA kernel is bound by that traffic.  Fewer tiles than
+//    that run on single CTAs (the remainder stream-K over every SM).
+//  - Whole tiles run in waves, so a GEMM whose tile count is just above a
+//    multiple of the slots (SMs, or co-resident pairs) idles most of them in
+//    its last wave (Llama-8B o_proj at 2048 tokens: 128 pair tiles of 256 on
+//    76 pairs = 1.7 waves).  The width taken is the one whose
+//    waves x (width + 16) is least (the 16 a per-tile cost, so that a narrower
+//    tile pays only when it saves a wave: 224 gives that o_proj 152 pair
+//    tiles, exactly 2 waves).
+// cfg.prefill_bn fixes the width, cfg.prefill_cta_pairs the kernel.
+struct PrefillChoice {
+  int bi;     // index into kPrefillBNs
+  bool pair;
+};
+
+int pair_slots(const tp_model* m, int epi) {
+  const GemmPlan p = plan_gemm(kSwapMaxTokens + 1, kPrefillBN, true);
+  return gemm_max_clusters(false, true, epi, 2, p.smem);
+}
+
+PrefillChoice choose_prefill(const tp_model* m, int epi, int64_t groups, int M, int rows) {
+  const int mode = m->cfg.prefill_cta_pairs;  // 0 auto, 1 always, 2 never
+  const int P = mode == 2 ? 0 : pair_slots(m, epi);
+  PrefillChoice ch;
+  ch.pair = P > 0 && (mode == 1 || groups * cdiv(M, 256) * cdiv(rows, kPrefillBN) >= P);
+  const int64_t G = ch.pair ? P : m->num_sms;
+  const int64_t a_tiles = cdiv(M, ch.pair ? 256 : 128);
+  ch.bi = 0;
+  if (m->cfg.prefill_bn) {
+    ch.bi = prefill_bn_index(m->cfg.prefill_bn);
+    return ch;
+  }
+  if (groups * a_tiles * cdiv(rows, kPrefillBNs[0]) < G) return ch;
+  int64_t best_cost = INT64_MAX;
+  for (int i = 0; i < kNumPrefillBN; ++i) {
+    const int64_t tiles = groups * a_tiles * cdiv(rows, kPrefillBNs[i]);
+    if (tiles < G) continue;
+    const int64_t cost = (tiles + G - 1) / G * (kPrefillBNs[i] + 16);
+    if (cost < best_cost) { best_cost = cost; ch.bi = i; }
+  }
+  return ch;
 }
 
 // Decode orientation: the flat (tile, K step) range is split evenly over the
@@ -191,6 +254,15 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
   a.cluster_split = 1;
+  if (p.pair) {
+    // CTA pairs: whole tiles, pair p takes tiles p, p + P, ...
+    a.pair = 1;
+    const int P = gemm_max_clusters(false, true, epi, 2, p.smem);
+    a.grid = 2 * (int)std::min<int64_t>(std::max(P, 1), n_tiles);
+    a.dp_waves = 0;
+    a.total_iters = 0;
+    return;
+  }
   // Up to 16 tokens the pieces are small (8 KB per 128-row tile) and
   // stream-K over every SM wins (measured, same box, alternating runs:
   // Llama-8B decode layer 111.5 -> 110.7 us); at 64 tokens the cluster split
@@ -202,7 +274,7 @@ void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
     // that many clusters are co-resident on this part's GPCs
     for (int s = 8; s >= 2; --s) {
       if (n_tiles * s > num_sms || n_tiles * s * 100 < (int64_t)num_sms * 65 || K < 2 * s) continue;
-      if (gemm_max_clusters(true, epi, s, p.smem) < n_tiles) continue;
+      if (gemm_max_clusters(true, false, epi, s, p.smem) < n_tiles) continue;
       a.cluster_split = s;
       a.dp_waves = 0;
       a.total_iters = 0;
@@ -248,7 +320,7 @@ size_t max_gemm_tiles(const tp_config_t& c, int M) {
     // decode orientation
     best = std::max(best, (size_t)t * cdiv(r, 128));
     // prefill orientation
-    best = std::max(best, (size_t)t * cdiv(M, 128) * cdiv(r, kPrefillBN));
+    best = std::max(best, (size_t)t * cdiv(M, 128) * cdiv(r, kPrefillBNs[kNumPrefillBN - 1]));
   }
   return best;
 }
@@ -308,7 +380,9 @@ tp_status prep_column(const tp_model* m, const ShardedLinear& W, const uint16_t*
                       int M, int epi, const EpiArgs& e, void* ws, const WsLayout& L, GemmArgs& a,
                       GemmPlan& p) {
   const int K = W.cols;
-  p = plan_gemm(M);
+  PrefillChoice ch{0, false};
+  if (M > kSwapMaxTokens) ch = choose_prefill(m, epi, W.ranks, M, W.rows);
+  p = plan_gemm(M, kPrefillBNs[ch.bi], ch.pair);
   memset(&a, 0, sizeof(a));
   bool ok;
   if (p.swap) {
@@ -324,8 +398,8 @@ tp_status prep_column(const tp_model* m, const ShardedLinear& W, const uint16_t*
     a.b_policy = 2;
   } else {
     ok = make_tmap(&a.tmA, x, K, M, 1, ldx * 2, (uint64_t)ldx * 2 * M, 128);
-    a.tmB = W.tm_b;
-    a.a_tiles = cdiv(M, 128);
+    a.tmB = p.pair ? W.tm_h[ch.bi] : W.tm_b[ch.bi];
+    a.a_tiles = cdiv(M, p.pair ? 256 : 128);
     a.b_tiles = cdiv(W.rows, p.BN);
     a.a_slice_mode = 0;
     a.b_slice_mode = 1;
@@ -369,7 +443,11 @@ tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
                    GemmArgs& a, GemmPlan& p, int& epi) {
   const tp_config_t& c = m->cfg;
   const int Kr = W.cols, H = W.rows, t = W.ranks;
-  p = plan_gemm(M);
+  // fused: one output group (the ranks are summed in K); unfused: t groups
+  PrefillChoice ch{0, false};
+  if (M > kSwapMaxTokens)
+    ch = choose_prefill(m, fused ? EPI_RESID : EPI_PARTIAL, fused ? 1 : t, M, H);
+  p = plan_gemm(M, kPrefillBNs[ch.bi], ch.pair);
   memset(&a, 0, sizeof(a));
   const uint64_t xs_bytes = (uint64_t)x_rank_stride * 2;
   bool ok;
@@ -384,8 +462,8 @@ tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
     a.b_policy = 2;
   } else {
     ok = make_tmap(&a.tmA, x, Kr, M, t, ldx * 2, xs_bytes, 128, &a.a_slice_mid);
-    a.tmB = W.tm_b;
-    a.a_tiles = cdiv(M, 128);
+    a.tmB = p.pair ? W.tm_h[ch.bi] : W.tm_b[ch.bi];
+    a.a_tiles = cdiv(M, p.pair ? 256 : 128);
     a.b_tiles = cdiv(H, p.BN);
     a.a_rows_valid = M;
     a.b_rows_valid = H;
@@ -476,7 +554,11 @@ tp_status alloc_linear(tp_model* m, ShardedLinear* L, int rows, int cols, int ra
   if (s != TP_OK) return s;
   const uint64_t rs = (uint64_t)cols * 2, ss = (uint64_t)rows * cols * 2;
   if (!make_tmap(&L->tm_a, L->data, cols, rows, ranks, rs, ss, 128)) return TP_ERR_CUDA;
-  if (!make_tmap(&L->tm_b, L->data, cols, rows, ranks, rs, ss, kPrefillBN)) return TP_ERR_CUDA;
+  for (int i = 0; i < kNumPrefillBN; ++i) {
+    if (!make_tmap(&L->tm_b[i], L->data, cols, rows, ranks, rs, ss, kPrefillBNs[i])) return TP_ERR_CUDA;
+    if (!make_tmap(&L->tm_h[i], L->data, cols, rows, ranks, rs, ss, kPrefillBNs[i] / 2))
+      return TP_ERR_CUDA;
+  }
   return TP_OK;
 }
 
@@ -503,25 +585,25 @@ struct MapUploader {
 // C ABI
 // ============================================================================
 namespace tpk {
-int gemm_max_clusters(bool swap, int epi, int cluster_x, size_t smem) {
-  // per (orientation, epilogue, cluster size, smem): the answer never changes
+int gemm_max_clusters(bool swap, bool pair, int epi, int cluster_x, size_t smem) {
+  // per (kernel, epilogue, cluster size, smem): the answer never changes
   static std::mutex mu;
   static std::vector<std::pair<uint64_t, int>> cache;
-  const uint64_t key = ((uint64_t)smem << 16) | ((uint64_t)cluster_x << 8) | ((uint64_t)epi << 1) |
-                       (swap ? 1u : 0u);
+  const uint64_t key = ((uint64_t)smem << 16) | ((uint64_t)cluster_x << 8) | ((uint64_t)epi << 2) |
+                       (pair ? 2u : 0u) | (swap ? 1u : 0u);
   std::lock_guard<std::mutex> lock(mu);
   for (auto& kv : cache)
     if (kv.first == key) return kv.second;
   int n = 0;
   switch (epi) {
-    case 0: n = gemm_max_clusters_epi0(swap, cluster_x, smem); break;
-    case 1: n = gemm_max_clusters_epi1(swap, cluster_x, smem); break;
-    case 2: n = gemm_max_clusters_epi2(swap, cluster_x, smem); break;
-    case 3: n = gemm_max_clusters_epi3(swap, cluster_x, smem); break;
-    case 4: n = gemm_max_clusters_epi4(swap, cluster_x, smem); break;
-    case 5: n = gemm_max_clusters_epi5(swap, cluster_x, smem); break;
-    case 6: n = gemm_max_clusters_epi6(swap, cluster_x, smem); break;
-    case 7: n = gemm_max_clusters_epi7(swap, cluster_x, smem); break;
+    case 0: n = gemm_max_clusters_epi0(swap, pair, cluster_x, smem); break;
+    case 1: n = gemm_max_clusters_epi1(swap, pair, cluster_x, smem); break;
+    case 2: n = gemm_max_clusters_epi2(swap, pair, cluster_x, smem); break;
+    case 3: n = gemm_max_clusters_epi3(swap, pair, cluster_x, smem); break;
+    case 4: n = gemm_max_clusters_epi4(swap, pair, cluster_x, smem); break;
+    case 5: n = gemm_max_clusters_epi5(swap, pair, cluster_x, smem); break;
+    case 6: n = gemm_max_clusters_epi6(swap, pair, cluster_x, smem); break;
+    case 7: n = gemm_max_clusters_epi7(swap, pair, cluster_x, smem); break;
   }
   cache.push_back({key, n});
   return n;
@@ -568,7 +650,8 @@ tp_status tp_config(tp_config_t* c) {
     return TP_ERR_ARG;
   const int t = c->t;
   if (c->attn_dp < 0 || c->host_io < 0 || c->host_io > 1 || c->plain_column_shards < 0 ||
-      c->plain_column_shards > 1)
+      c->plain_column_shards > 1 || (c->prefill_bn != 0 && prefill_bn_index(c->prefill_bn) < 0) ||
+      c->prefill_cta_pairs < 0 || c->prefill_cta_pairs > 2)
     return TP_ERR_ARG;
   if (c->attn_dp == 0) c->attn_dp = 1;
   if (t % c->attn_dp) return TP_ERR_DIVISIBILITY;

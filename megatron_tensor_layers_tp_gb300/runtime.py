@@ -27,7 +27,8 @@ def _stream(stream) -> int:
 
 def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, n_layers, t,
                 rms_eps=1e-5, rope_theta=10000.0, max_positions=8192,
-                attn_dp=1, host_io=0, plain_column_shards=0) -> B.tp_config_t:
+                attn_dp=1, host_io=0, plain_column_shards=0, prefill_bn=0,
+                prefill_cta_pairs=0) -> B.tp_config_t:
     c = B.tp_config_t()
     c.hidden, c.n_heads, c.n_kv_heads, c.head_dim = hidden, n_heads, n_kv_heads, head_dim
     c.intermediate, c.vocab, c.n_layers, c.t = intermediate, vocab, n_layers, t
@@ -35,6 +36,8 @@ def make_config(hidden, n_heads, n_kv_heads, head_dim, intermediate, vocab, n_la
     c.attn_dp = attn_dp
     c.host_io = host_io
     c.plain_column_shards = plain_column_shards
+    c.prefill_bn = prefill_bn
+    c.prefill_cta_pairs = prefill_cta_pairs
     return c
 
 

@@ -86,17 +86,19 @@ def to_f64(t) -> np.ndarray:
 
 
 def build_model(w: Workload, t: int, layers: int = None, with_head: bool = None, max_tokens=None,
-                attn_dp: int = 1, host_io: int = 0, plain_column_shards: int = 0):
+                attn_dp: int = 1, host_io: int = 0, plain_column_shards: int = 0,
+                prefill_bn: int = 0, prefill_cta_pairs: int = 0):
     """Device weights + TPModel for workload w at t ranks (attention over
-    t / attn_dp ranks per DP group); host_io and plain_column_shards as in
-    tp_config_t."""
+    t / attn_dp ranks per DP group); host_io, plain_column_shards,
+    prefill_bn and prefill_cta_pairs as in tp_config_t."""
     import torch
     from megatron_tensor_layers_tp_gb300.runtime import TPModel, make_config
     n_layers = w.n_layers if layers is None else layers
     head = w.with_embed if with_head is None else with_head
     cfg = make_config(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab,
                       n_layers, t, w.rms_eps, w.rope_theta, max_positions=max(w.l_max, 16),
-                      attn_dp=attn_dp, host_io=host_io, plain_column_shards=plain_column_shards)
+                      attn_dp=attn_dp, host_io=host_io, plain_column_shards=plain_column_shards,
+                      prefill_bn=prefill_bn, prefill_cta_pairs=prefill_cta_pairs)
     dev_layers = []
     for l in range(n_layers):
         dev_layers.append(device_layer(w, l))

@@ -69,6 +69,16 @@ def test_config_rejections_have_the_named_status():
     assert B.tp_config(ok) == B.TP_OK
     assert (ok.q_heads_per_rank, ok.kv_heads_per_rank, ok.inter_per_rank, ok.vocab_per_rank) == \
         (4, 1, 1792, 16032)
+    for bn, want in ((0, B.TP_OK), (224, B.TP_OK), (128, B.TP_OK), (100, ST["TP_ERR_ARG"]),
+                     (240, ST["TP_ERR_ARG"]), (-256, ST["TP_ERR_ARG"])):
+        c = _cfg(32, 8, 14336, 128256, 8)
+        c.prefill_bn = bn
+        assert B.tp_config(c) == want, bn
+    for mode, want in ((0, B.TP_OK), (1, B.TP_OK), (2, B.TP_OK), (3, ST["TP_ERR_ARG"]),
+                       (-1, ST["TP_ERR_ARG"])):
+        c = _cfg(32, 8, 14336, 128256, 8)
+        c.prefill_cta_pairs = mode
+        assert B.tp_config(c) == want, mode
 
 
 def test_calls_without_a_model_are_rejected_on_the_host():

@@ -24,9 +24,9 @@ def _wl(hidden=512, n_heads=8, n_kv=2, head_dim=64, inter=1536, vocab=1001, seed
                           4, 1, 8, True, seed=seed, norm_weight_sigma=norm_sigma)
 
 
-def _model(w, t, head=True):
+def _model(w, t, head=True, prefill_cta_pairs=0):
     cfg = make_config(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab, 1, t,
-                      max_positions=4096, plain_column_shards=1)
+                      max_positions=4096, plain_column_shards=1, prefill_cta_pairs=prefill_cta_pairs)
     layers = [device_layer(w, 0)]
     emb = lm = fn = None
     if head:
@@ -230,6 +230,53 @@ def test_prefill_orientation_schedules_match_oracle(M, inter, t):
     assert rel_err(to_f64(out), ref) <= TOL
     assert m.check_device() == 0
     m.close()
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+@pytest.mark.parametrize("M", [65, 200, 300, 1100])
+def test_cta_pair_gemms_match_oracle(t, M):
+    # every GEMM above 64 tokens on CTA pairs (256-row tiles; M=65 and 200 a
+    # single ragged pair tile whose odd CTA holds no or few tokens, 1100 five
+    # tiles), each epilogue of the prefill orientation against the oracle,
+    # and against the single-CTA kernel
+    w = _wl(hidden=512, n_heads=8, n_kv=2, head_dim=64, inter=1536)
+    mp, _, lm = _model(w, t, prefill_cta_pairs=1)
+    ms, _, _ = _model(w, t, prefill_cta_pairs=2)
+    W = oracle_layer(w, 0)
+    dims = O.Dims(w.hidden, w.n_heads, w.n_kv_heads, w.head_dim, w.intermediate, w.vocab)
+    p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)
+    x = _x(M, w.hidden, seed=51)
+    xf = to_f64(x)
+    for which, shards in ((B.TP_QKV, O.shard_qkv(W, dims, p)), (B.TP_GATE_UP, O.shard_gate_up(W, p))):
+        y = mp.column_linear(0, which, x)
+        ys = ms.column_linear(0, which, x)
+        for r, sh in enumerate(shards):
+            ref = O.linear(xf, sh)
+            assert rel_err(to_f64(y[r]), ref) <= TOL, (which, r)
+            assert rel_err(to_f64(y[r]), to_f64(ys[r])) <= TOL, (which, r)
+    for which, Wfull in ((B.TP_O, W.wo), (B.TP_DOWN, W.wd)):
+        K = Wfull.shape[1]
+        a = _x(M, K, seed=52)
+        res = _x(M, w.hidden, seed=53)
+        partials = [O.linear(xs, Ws) for xs, Ws in zip(O.shard_rows_by_input(to_f64(a), t),
+                                                        O.shard_rows_by_input(Wfull, t))]
+        ref = O.round_bf16(to_f64(res) + O.all_reduce_sum(partials))
+        for fused in (True, False):
+            y = mp.row_linear_reduce(0, which, a, residual=res, fused=fused)
+            assert rel_err(to_f64(y), ref) <= TOL, (which, fused)
+    logits = mp.lm_head_gather(x)
+    ref = O.sharded_lm_head(xf, O.shard_vocab(to_f64(lm), p), w.vocab)
+    assert rel_err(to_f64(logits), ref) <= TOL
+    assert mp.check_device() == 0 and ms.check_device() == 0
+    mp.close()
+    ms.close()
+
+
+def test_cta_pair_config_values():
+    w = _wl()
+    for mode in (0, 1, 2):
+        m, _, _ = _model(w, 2, head=False, prefill_cta_pairs=mode)
+        m.close()
 
 
 @pytest.mark.parametrize("t", [1, 2, 8])

@@ -109,8 +109,9 @@ def test_ragged_prefill_matches_oracle():
     model.close()
 
 
-def _ragged_prefill(w, t, lens, seed, fused=True):
-    model, _, _ = build_model(w, t, max_tokens=sum(lens))
+def _ragged_prefill(w, t, lens, seed, fused=True, prefill_bn=0, prefill_cta_pairs=0):
+    model, _, _ = build_model(w, t, max_tokens=sum(lens), prefill_bn=prefill_bn,
+                              prefill_cta_pairs=prefill_cta_pairs)
     n = len(lens)
     ks = [model.alloc_kv(n, w.ctx)]
     vs = [model.alloc_kv(n, w.ctx)]
@@ -157,6 +158,32 @@ def test_norm_paths_above_32_tokens(fused):
     err, launches = _ragged_prefill(w, 2, [16, 16, 16], 7, fused=fused)
     assert err <= LAYER_TOL
     assert launches == (6 if fused else 9)
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192, 160, 128])
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("pairs", [2, 1])
+def test_prefill_tile_widths_match_oracle(bn, fused, pairs):
+    # 2100 tokens (17 row tiles of 128, 9 of 256, the last ragged) at every
+    # output-feature tile width, on single CTAs (pairs=2: at t=2 gate_up has
+    # 2 x 17 x ceil(1536/bn) >= 152 tiles, whole-tile waves plus a last partial
+    # wave; qkv and o_proj fewer than 152, stream-K) and on CTA pairs
+    # (pairs=1); widths that do not divide 384 (qkv rows per rank), 1536 or
+    # 512 leave a last tile of each rank partly outside the weight
+    w = _wl("prefill", n_seqs=3, seq_len=1000, ctx=1000)
+    err, _ = _ragged_prefill(w, 2, [700, 1000, 400], 8, fused=fused, prefill_bn=bn,
+                             prefill_cta_pairs=pairs)
+    assert err <= LAYER_TOL
+
+
+@pytest.mark.parametrize("t", [1, 4])
+@pytest.mark.parametrize("fused", [True, False])
+def test_prefill_layer_on_cta_pairs_matches_oracle(t, fused):
+    # short ragged sequences (one pair tile whose odd CTA is idle) and longer
+    w = _wl("prefill", n_seqs=3, seq_len=300, ctx=300)
+    for lens in ([3, 70, 8], [300, 17, 260]):
+        err, _ = _ragged_prefill(w, t, lens, 9, fused=fused, prefill_cta_pairs=1)
+        assert err <= LAYER_TOL, lens
 
 
 def test_sharded_equals_unsharded_on_gpu():
