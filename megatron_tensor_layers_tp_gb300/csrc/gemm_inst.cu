@@ -42,7 +42,8 @@ cudaError_t TPK_CAT(launch_gemm_epi, TPK_EPI)(bool swap, const GemmArgs& a, size
   if (e != cudaSuccess) return e;
   if (pair) {
     if constexpr (kHasPair)
-      return launch_kc(gemm_pair_kernel<TPK_EPI>, dim3(a.grid), dim3(kPairThreads), smem, st, 2, a);
+      return launch_kc(gemm_pair_kernel<TPK_EPI>, dim3(a.grid), dim3(kPairThreads<TPK_EPI>), smem, st,
+                       2, a);
     return cudaErrorInvalidValue;
   }
   const int cx = a.cluster_split > 1 ? a.cluster_split : 1;
@@ -59,7 +60,7 @@ int TPK_CAT(gemm_max_clusters_epi, TPK_EPI)(bool swap, bool pair, int cluster_x,
   if (prepare(swap, pair) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster_x * 64);
-  cfg.blockDim = dim3(pair ? kPairThreads : (swap ? kThreadsOf<true> : kThreadsOf<false>));
+  cfg.blockDim = dim3(pair ? kPairThreads<TPK_EPI> : (swap ? kThreadsOf<true> : kThreadsOf<false>));
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -172,10 +172,13 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
       for (int j = 0; j < 16; ++j) in.r[j] = 0.f;
     }
   } else if constexpr (!SWAP && EPI == EPI_QKV) {
+    // pos[0]: the token's position, pos[1]: its sequence (K/V rows only)
     const int m = arow, f0 = brow0;
-    in.pos[0] = (m < e.M && f0 < a.b_rows_valid) ? e.positions[m] : -1;
     int kind, head, w;
     qkv_classify(e, f0, kind, head, w);
+    const bool mval = m < e.M && f0 < a.b_rows_valid;
+    in.pos[0] = mval ? e.positions[m] : -1;
+    in.pos[1] = (mval && kind != 0) ? e.token_seq[m] : 0;
     const bool ok = in.pos[0] >= 0 && in.pos[0] < e.l_max && kind != 2;
     const float2* cs = e.rope + (int64_t)(ok ? in.pos[0] : 0) * (e.head_dim / 2) + (w >> 1);
 #pragma unroll
@@ -423,7 +426,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
         *reinterpret_cast<uint4*>(dst + c_lo) = lo;
         *reinterpret_cast<uint4*>(dst + c_hi) = hi;
       } else if ((g % e.kv_replicas) == 0) {
-        const int seq = e.token_seq[m];
+        const int seq = in.pos[1];
         uint16_t* cache = kind == 1 ? e.k_cache : e.v_cache;
         uint16_t* dst = cache + (int64_t)(g / e.kv_replicas) * e.kv_copy_stride +
                         (((int64_t)seq * e.kv_heads_per_rank + head) * e.l_max + pos) * d;

@@ -10,22 +10,31 @@
 // every tile width), the pair halves the weight part of it.
 //
 // Work: whole tiles in waves, pair p taking tiles p, p + P, ... (P pairs).
-// Roles as in the single-CTA kernel: warp 0 loads (both CTAs), warp 1 of the
-// even CTA issues the MMAs, warps 2-5 of both CTAs drain their accumulators
-// through the same fused epilogues.  Barriers: the even CTA's full[s] counts
-// both CTAs' bytes; each commit arrives on empty[s] / acc_full[b] of both
-// CTAs; the even CTA's acc_empty[b] takes the epilogue warps of both.  Every
-// wait is bounded.
+// Roles: warp 0 loads (both CTAs), warp 1 of the even CTA issues the MMAs,
+// the epilogue warps of both CTAs drain their accumulators through the fused
+// epilogues of the single-CTA kernel.  The last tile's epilogue is not hidden
+// behind a mainloop (with four warps it took 6-12 us of a 55-275 us GEMM), so
+// eight warps run it, two per TMEM lane quadrant on alternate 16-column units
+// (measured, same box: Llama-8B prefill o_proj 60.0 -> 58.3 us, gate_up and
+// down 1 us less); the qkv epilogue keeps four (its stores then overlap the
+// next tile's loads less: 81.7 -> 83.6 us with eight).  Barriers: the even
+// CTA's full[s] counts both CTAs' bytes; each commit arrives on empty[s] /
+// acc_full[b] of both CTAs; the even CTA's acc_empty[b] takes the epilogue
+// warps of both.  Every wait is bounded.
 #pragma once
 #include "gemm_kernel.cuh"
 
 namespace tpk {
 
-constexpr int kPairThreads = kThreadsOf<false>;  // 192: loader, MMA, 4 epilogue warps
+template <int EPI>
+constexpr int kPairEpiWarps = EPI == EPI_QKV ? 4 : 8;
+template <int EPI>
+constexpr int kPairThreads = (2 + kPairEpiWarps<EPI>) * 32;  // loader, MMA, epilogue warps
 
 template <int EPI>
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(kPairThreads<EPI>, 1)
     gemm_pair_kernel(const __grid_constant__ GemmArgs a) {
+  constexpr int NH = kPairEpiWarps<EPI> / 4;  // epilogue warps per TMEM lane quadrant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -48,7 +57,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 2 * 4);  // the epilogue warps of both CTAs
+      mbar_init(&acc_empty[i], 2 * kPairEpiWarps<EPI>);  // the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -171,8 +180,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   } else {
     pdl_wait();
     if constexpr (kLateSignal) pdl_launch_dependents();
-    // epilogue warp w reads TMEM lanes of quadrant w % 4: token rows of this CTA
+    // epilogue warp w reads TMEM lanes of quadrant w % 4 (token rows of this
+    // CTA) and the 16-column units half, half + NH, ... of the tile
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     const int* tok = nullptr;  // token tables live in EpiArgs in this orientation
@@ -188,11 +199,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
       const int arow = ia * 256 + static_cast<int>(rank) * 128 + row;
       const int brow = ib * BN;
-      // inputs of chunk c0 + 16 are fetched before chunk c0 is stored
+      // inputs of the next unit are fetched before the current one is stored
       EpiIn cur, nxt;
-      epi_load<false, EPI>(a, g, arow, brow, tok, cur);
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        if (c0 + 16 < BN) epi_load<false, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
+      const int c_first = half * 16;
+      if (c_first < BN) epi_load<false, EPI>(a, g, arow, brow + c_first, tok, cur);
+      for (int c0 = c_first; c0 < BN; c0 += NH * 16) {
+        if (c0 + NH * 16 < BN) epi_load<false, EPI>(a, g, arow, brow + c0 + NH * 16, tok, nxt);
         float v[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
