@@ -558,14 +558,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 constexpr int kPreThreads = 128;
 constexpr int kPreStages = 2;
 
+// Shared memory is the K/V ring alone (the Q fragments go straight from
+// global memory to registers), so that three CTAs fit on an SM: the kernel is
+// latency-bound (each CTA walks at most a few key tiles), and with 32-key
+// score sub-tiles its registers also allow three.
 template <int D>
 struct PreSmem {
   static constexpr int kTileBytes = (D / 64) * 8192;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kQRow = D * 2 + 16;
-  static constexpr size_t bytes() {
-    return 1024 + (size_t)kPreStages * kStageBytes + 64 * kQRow + 128;
-  }
+  static constexpr size_t bytes() { return 1024 + (size_t)kPreStages * kStageBytes + 128; }
 };
 
 template <int D>
@@ -575,8 +576,7 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* tiles = smem;
-  uint8_t* sQ = tiles + kPreStages * L::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + 64 * L::kQRow);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + kPreStages * L::kStageBytes);
   int* flags = reinterpret_cast<int*>(full + kPreStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -600,13 +600,6 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
     for (int i = 0; i < nrows; ++i) mx = max(mx, a.positions[q0 + i]);
     flags[0] = mx;
   }
-  // stage q rows
-  for (int i = threadIdx.x; i < 64 * (D / 8); i += kPreThreads) {
-    const int row = i / (D / 8), ch = i % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < nrows) v = *reinterpret_cast<const uint4*>(a.q + (int64_t)(q0 + row) * a.ld_q + (int64_t)h * D + ch * 8);
-    *reinterpret_cast<uint4*>(sQ + row * L::kQRow + ch * 16) = v;
-  }
   __syncthreads();
   const int max_pos = min(flags[0], a.l_max - 1);
   const int n_tiles = max_pos / kKeyTile + 1;
@@ -624,9 +617,23 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
   if (threadIdx.x == 0)
     for (int i = 0; i < min(kPreStages, n_tiles); ++i) issue(i);
 
-  uint32_t qa[D / 16][4];
-  load_q_frags<D>(smem_u32(sQ) + warp * 16 * L::kQRow, L::kQRow, qa);
+  // A fragments of the warp's 16 query rows (m16n8k16 layout: rows r0 and
+  // r0 + 8, column pairs c2 and c2 + 8 of every 16-wide K step)
   const int r0 = warp * 16 + (lane >> 2);
+  uint32_t qa[D / 16][4];
+  {
+    const int c2 = (lane & 3) * 2;
+    const uint16_t* q_lo = a.q + (int64_t)(q0 + r0) * a.ld_q + (int64_t)h * D + c2;
+    const uint16_t* q_hi = q_lo + 8 * a.ld_q;
+    const bool v_lo = r0 < nrows, v_hi = r0 + 8 < nrows;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = v_lo ? *reinterpret_cast<const uint32_t*>(q_lo + kk * 16) : 0u;
+      qa[kk][1] = v_hi ? *reinterpret_cast<const uint32_t*>(q_hi + kk * 16) : 0u;
+      qa[kk][2] = v_lo ? *reinterpret_cast<const uint32_t*>(q_lo + kk * 16 + 8) : 0u;
+      qa[kk][3] = v_hi ? *reinterpret_cast<const uint32_t*>(q_hi + kk * 16 + 8) : 0u;
+    }
+  }
   int lim[2];
   lim[0] = r0 < nrows ? a.positions[q0 + r0] : -1;
   lim[1] = r0 + 8 < nrows ? a.positions[q0 + r0 + 8] : -1;
@@ -652,7 +659,10 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
     const int key0 = tile * kKeyTile;
     if (key0 <= warp_max) {
       const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
-      attn_tile<D, 8>(qa, st, st + L::kTileBytes, 0, key0, lim, a.scale_log2, m, l, o);
+      // two 32-key halves: fewer live score registers than one 64-key pass
+      attn_tile<D, 4>(qa, st, st + L::kTileBytes, 0, key0, lim, a.scale_log2, m, l, o);
+      if (key0 + 32 <= warp_max)
+        attn_tile<D, 4>(qa, st, st + L::kTileBytes, 32, key0 + 32, lim, a.scale_log2, m, l, o);
     }
     __syncthreads();
     if (threadIdx.x == 0 && tile + kPreStages < n_tiles) issue(tile + kPreStages);
