@@ -26,8 +26,8 @@ def _wl(mode, n_seqs, seq_len, ctx, hidden=512, n_heads=8, n_kv=2, head_dim=64, 
                           bias=True, sigma_b=0.5)
 
 
-def _layer(w, t, fused=True):
-    model, _, _ = build_model(w, t)
+def _layer(w, t, fused=True, pairs=0):
+    model, _, _ = build_model(w, t, prefill_cta_pairs=pairs)
     batch, caches = make_batch(model, w)
     h = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
     synth.fill_normal_(h, w.seed, synth.tensor_id("hidden"), w.sigma_h)
@@ -62,9 +62,11 @@ def test_decode_layer_with_biases_matches_oracle(t, n_kv, fused):
 
 
 @pytest.mark.parametrize("t", [1, 4])
-def test_prefill_layer_with_biases_matches_oracle(t):
+@pytest.mark.parametrize("pairs", [0, 1, 2])
+def test_prefill_layer_with_biases_matches_oracle(t, pairs):
+    # pairs: 0 chosen per GEMM (single CTAs at this size), 1 CTA pairs, 2 single CTAs
     w = _wl("prefill", n_seqs=3, seq_len=70, ctx=70)
-    model, h = _layer(w, t)
+    model, h = _layer(w, t, pairs=pairs)
     assert rel_err(to_f64(h), _oracle(w)) <= LAYER_TOL
     model.close()
 
@@ -82,10 +84,10 @@ def test_biased_sharded_equals_unsharded_on_gpu():
 
 
 @pytest.mark.parametrize("t", [2, 4])
-@pytest.mark.parametrize("M", [16, 200])
-def test_column_and_row_calls_carry_their_biases(t, M):
+@pytest.mark.parametrize("M,pairs", [(16, 0), (200, 0), (200, 1), (600, 1)])
+def test_column_and_row_calls_carry_their_biases(t, M, pairs):
     w = _wl("decode", n_seqs=4, seq_len=1, ctx=8)
-    model, _, _ = build_model(w, t, max_tokens=M, plain_column_shards=1)
+    model, _, _ = build_model(w, t, max_tokens=M, plain_column_shards=1, prefill_cta_pairs=pairs)
     W = oracle_layer(w, 0)
     dims = oracle_dims(w)
     p = O.plan(w.n_heads, w.n_kv_heads, w.intermediate, w.vocab, t)

@@ -23,8 +23,8 @@ def _wl(mode, n_seqs, seq_len, ctx, n_heads=8, n_kv=2, layers=1, embed=False, bi
                           bias=bias)
 
 
-def _run(w, t, attn_dp, fused=True):
-    model, _, _ = build_model(w, t, attn_dp=attn_dp)
+def _run(w, t, attn_dp, fused=True, pairs=0):
+    model, _, _ = build_model(w, t, attn_dp=attn_dp, prefill_cta_pairs=pairs)
     batch, caches = make_batch(model, w)
     h = torch.empty((w.tokens, w.hidden), dtype=torch.bfloat16, device="cuda")
     synth.fill_normal_(h, w.seed, synth.tensor_id("hidden"), w.sigma_h)
@@ -66,9 +66,10 @@ def test_decode_layer_with_dp_attention_matches_oracle(t, attn_dp, n_kv, fused):
 
 
 @pytest.mark.parametrize("t,attn_dp", [(4, 2), (8, 4)])
-def test_prefill_layer_with_dp_attention_matches_oracle(t, attn_dp):
+@pytest.mark.parametrize("pairs", [0, 1])
+def test_prefill_layer_with_dp_attention_matches_oracle(t, attn_dp, pairs):
     w = _wl("prefill", n_seqs=4, seq_len=70, ctx=70, bias=True)
-    model, h, _ = _run(w, t, attn_dp)
+    model, h, _ = _run(w, t, attn_dp, pairs=pairs)
     kc, vc = oracle_caches(w, 0, range(w.n_seqs))
     ref = O.layer_forward(synth.host_hidden(w), oracle_layer(w, 0), kc, vc, oracle_batch(w),
                           oracle_dims(w))

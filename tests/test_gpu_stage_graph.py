@@ -157,6 +157,31 @@ def test_graph_forward_replays_eager(t):
     model.close()
 
 
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_graph_prefill_forward_replays_eager(pairs):
+    # a prefill forward (2 x 40 tokens, above the decode orientation) captured
+    # with its GEMMs on CTA pairs (cluster launches, pairs = 1) or single CTAs
+    w = synth.Workload("unit-stages-prefill", 256, 4, 2, 64, 768, 1001, 2, (1,), "prefill", 2,
+                       40, 40, True, seed=9, norm_weight_sigma=0.1)
+    model, _, _ = build_model(w, 2, prefill_cta_pairs=pairs)
+    batch, _ = make_batch(model, w)
+    ids_np = synth.token_ids(w)
+    ids = torch.from_numpy(ids_np).cuda()
+    h_ref, logits_ref = _eager(model, w, batch, ids)
+    stream = torch.cuda.Stream()
+    h = torch.empty_like(h_ref)
+    logits = torch.empty_like(logits_ref)
+    graph = model.capture_forward(ids, batch, h, logits, stream)
+    graph.launch(stream)
+    stream.synchronize()
+    assert model.check_device() == 0
+    assert torch.equal(_bits(logits), _bits(logits_ref))
+    assert torch.equal(_bits(h), _bits(h_ref))
+    assert rel_err(to_f64(logits), oracle_forward(w, ids_np)) <= LOGIT_TOL
+    graph.close()
+    model.close()
+
+
 def test_graph_layer_replays_eager_at_decode_shape():
     # one Llama-3.1-8B-shaped layer at t = 8, 16 sequences, 256-token context
     w = synth.Workload("unit-graph-layer", 4096, 32, 8, 128, 14336, 1000, 1, (8,), "decode", 16,
