@@ -14,7 +14,7 @@ namespace tpk {
 #define TPK_CAT(a, b) TPK_CAT2(a, b)
 
 // the pair kernel serves the epilogues of the prefill orientation
-constexpr bool kHasPair = TPK_EPI != EPI_RESID_SQ && TPK_EPI != EPI_QKV_PIECES;
+constexpr bool kHasPair = TPK_EPI != EPI_QKV_PIECES;
 
 template <typename F>
 static cudaError_t set_smem_attr(F* kernel, bool& done) {

@@ -88,7 +88,28 @@ struct EpiIn {
   int pos[16];
   float2 cs[16];
   float b[16];  // output bias: one value per row (decode) or per column (prefill)
+  float rs;     // prefill orientation, folded RMSNorm: the token's 1/rms (set by the caller)
 };
+
+// Prefill orientation, folded RMSNorm (norm_mode 2): token m's 1/rms from the
+// sums of squares the kernel that wrote h left (norm_slots per token, fixed
+// order); 1 for any other norm mode.
+// (norm_slots is a multiple of 4: a row's slots are read as 16-byte vectors,
+// eight in flight together)
+__device__ __forceinline__ float prefill_row_rs(const EpiArgs& e, int m) {
+  if (e.norm_mode != 2 || m >= e.M) return 1.f;
+  const float4* p = reinterpret_cast<const float4*>(e.norm_partials + (int64_t)m * e.norm_slots);
+  const int n4 = e.norm_slots >> 2;
+  float ss = 0.f;
+  for (int i0 = 0; i0 < n4; i0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = i0 + k < n4 ? __ldcg(p + i0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+  }
+  return 1.0f / sqrtf(ss / (float)e.norm_width + e.norm_eps);
+}
 
 // Epilogues that add the GEMM's output bias (the unfused row-parallel
 // partials leave it to the rank reduction; the LM head has none).
@@ -186,15 +207,22 @@ __device__ __forceinline__ void epi_load(const GemmArgs& a, int g, int arow, int
   }
 }
 
+// Returns, in the prefill orientation with EPI_RESID_SQ, the sum of the
+// squares of the 16 values it stored (0 otherwise).
 template <bool SWAP, int EPI>
-__device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
-                                          const int* tok, float (&v)[16], const EpiIn& in) {
+__device__ __forceinline__ float epi_chunk(const GemmArgs& a, int g, int arow, int brow0,
+                                           const int* tok, float (&v)[16], const EpiIn& in) {
   const EpiArgs& e = a.e;
   if constexpr (SWAP && kEpiNorm<EPI>) {
     if (e.norm_mode) {  // the token's 1/rms, staged in shared memory after tok
       const float* rs = reinterpret_cast<const float*>(tok + 4 * kSwapMaxTokens);
 #pragma unroll
       for (int j = 0; j < kUnit<SWAP>; ++j) v[j] *= rs[brow0 + j];
+    }
+  } else if constexpr (!SWAP && kEpiNorm<EPI>) {
+    if (e.norm_mode == 2) {  // the token's 1/rms, fetched by the caller once per tile
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] *= in.rs;
     }
   }
   if constexpr (kEpiBias<EPI>) {
@@ -319,7 +347,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
   } else {
     const int m = arow;
     const int f0 = brow0;
-    if (m >= e.M || f0 >= a.b_rows_valid) return;
+    if (m >= e.M || f0 >= a.b_rows_valid) return 0.f;
     if constexpr (kResid<EPI>) {
       uint16_t* out = static_cast<uint16_t*>(e.out) + (int64_t)m * e.ld_out + f0;
       const float* r = in.r;
@@ -333,6 +361,20 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       }
       reinterpret_cast<uint4*>(out)[0] = o0;
       reinterpret_cast<uint4*>(out)[1] = o1;
+      if constexpr (EPI == EPI_RESID_SQ) {
+        // the squares of the stored values, for the next RMSNorm
+        float sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w[2] = {p0[j], p1[j]};
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xFFFF0000u);
+            sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+          }
+        }
+        return sq;
+      }
     } else if constexpr (EPI == EPI_PARTIAL) {
       float4* out = reinterpret_cast<float4*>(static_cast<float*>(e.out) +
                                               (int64_t)g * e.out_group_stride +
@@ -395,7 +437,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       qkv_classify(e, f0, kind, head, w);
       const int d = e.head_dim, half = d / 2;
       const int pos = in.pos[0];
-      if (pos < 0 || pos >= e.l_max) return;  // never index the cache or table out of range
+      if (pos < 0 || pos >= e.l_max) return 0.f;  // never index the cache or table out of range
       float outv[16];
       if (kind == 2) {
 #pragma unroll
@@ -435,6 +477,22 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& a, int g, int arow, in
       }
     }
   }
+  return 0.f;
+}
+
+// Prefill orientation, EPI_RESID_SQ: token m's sum of squares over its units
+// of output tile ib of b_tiles (half: which of two threads sharing the tile;
+// whole: one thread covered the whole tile, so the other slot is zero).  The
+// last tile's writers also zero the padding up to sq_ld (a multiple of 4).
+__device__ __forceinline__ void store_row_sq(const GemmArgs& a, int m, int ib, int half, float ss,
+                                             bool whole) {
+  const EpiArgs& e = a.e;
+  if (!e.sq_out || m >= e.M) return;
+  float* row = e.sq_out + (int64_t)m * e.sq_ld;
+  row[2 * ib + half] = ss;
+  if (whole) row[2 * ib + 1] = 0.f;
+  if (ib == a.b_tiles - 1 && half == 0)
+    for (int i = 2 * a.b_tiles; i < e.sq_ld; ++i) row[i] = 0.f;
 }
 
 // --------------------------------------------------------------------------
@@ -829,16 +887,23 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
           }
         } else {
           // inputs of chunk c0 + 16 are fetched before chunk c0 is stored
+          float rs = 1.f, ss = 0.f;
+          if constexpr (kEpiNorm<EPI>) rs = prefill_row_rs(a.e, arow);
           EpiIn cur, nxt;
           epi_load<SWAP, EPI>(a, g, arow, brow, tok, cur);
+          cur.rs = rs;
           for (int c0 = 0; c0 < BN; c0 += 16) {
-            if (c0 + 16 < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
+            if (c0 + 16 < BN) {
+              epi_load<SWAP, EPI>(a, g, arow, brow + c0 + 16, tok, nxt);
+              nxt.rs = rs;
+            }
             float v[16];
             tld(taddr + c0, v);
             tmem_ld_wait();
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, cur);
+            ss += epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, cur);
             cur = nxt;
           }
+          if constexpr (EPI == EPI_RESID_SQ) store_row_sq(a, arow, ib, 0, ss, true);
         }
         tc_fence_before();
         __syncwarp();
@@ -894,11 +959,17 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
           };
           const int cs = NH * U;  // this thread's units: half * U, + cs, ...
           load_batch(half * U, 0);
+          // prefill orientation: the token's 1/rms (folded norm) and its sum of
+          // squares over the tile (EPI_RESID_SQ; one thread covers the tile)
+          float rs = 1.f, ss = 0.f;
+          if constexpr (!SWAP && kEpiNorm<EPI>) rs = prefill_row_rs(a.e, arow);
           EpiIn in;  // inputs of the current unit; those of the next are fetched ahead
           if (use_pre) in = pre;
           else epi_load<SWAP, EPI>(a, g, arow, brow + half * U, tok, in);
+          in.rs = rs;
           for (int c0 = half * U; c0 < BN; c0 += cs) {
             EpiIn nxt;
+            nxt.rs = rs;
             if constexpr (kEpiAhead<EPI>)
               if (c0 + cs < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cs, tok, nxt);
             float v[16];
@@ -914,10 +985,12 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
               if (s0 + 4 < nseg) load_batch(c0, s0 + 4);
               else if (c0 + cs < BN) load_batch(c0 + cs, 0);
             }
-            epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
+            ss += epi_chunk<SWAP, EPI>(a, g, arow, brow + c0, tok, v, in);
             if constexpr (kEpiAhead<EPI>) in = nxt;
             else if (c0 + cs < BN) epi_load<SWAP, EPI>(a, g, arow, brow + c0 + cs, tok, in);
+            in.rs = rs;
           }
+          if constexpr (!SWAP && EPI == EPI_RESID_SQ) store_row_sq(a, arow, ib, 0, ss, true);
           if (threadIdx.x == 64) a.tickets[sg.tile] = 0;
         }
         bar_sync(1, ET);

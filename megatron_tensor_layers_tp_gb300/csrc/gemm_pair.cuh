@@ -199,18 +199,27 @@ __global__ void __launch_bounds__(kPairThreads<EPI>, 1)
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN;
       const int arow = ia * 256 + static_cast<int>(rank) * 128 + row;
       const int brow = ib * BN;
-      // inputs of the next unit are fetched before the current one is stored
+      // inputs of the next unit are fetched before the current one is stored;
+      // the token's 1/rms (folded norm) once per tile, its sum of squares over
+      // this thread's units (EPI_RESID_SQ)
+      float rs = 1.f, ss = 0.f;
+      if constexpr (kEpiNorm<EPI>) rs = prefill_row_rs(a.e, arow);
       EpiIn cur, nxt;
       const int c_first = half * 16;
       if (c_first < BN) epi_load<false, EPI>(a, g, arow, brow + c_first, tok, cur);
+      cur.rs = rs;
       for (int c0 = c_first; c0 < BN; c0 += NH * 16) {
-        if (c0 + NH * 16 < BN) epi_load<false, EPI>(a, g, arow, brow + c0 + NH * 16, tok, nxt);
+        if (c0 + NH * 16 < BN) {
+          epi_load<false, EPI>(a, g, arow, brow + c0 + NH * 16, tok, nxt);
+          nxt.rs = rs;
+        }
         float v[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
-        epi_chunk<false, EPI>(a, g, arow, brow + c0, tok, v, cur);
+        ss += epi_chunk<false, EPI>(a, g, arow, brow + c0, tok, v, cur);
         cur = nxt;
       }
+      if constexpr (EPI == EPI_RESID_SQ) store_row_sq(a, arow, ib, half, ss, NH == 1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty0 + buf * 8);

@@ -55,7 +55,8 @@ struct EpiArgs {
   // value of output row f of rank g is bias[g * bias_group_stride + f]
   const uint16_t* bias;
   int64_t bias_group_stride;
-  // RMSNorm folded into the GEMM (decode orientation, QKV and SILU): the
+  // RMSNorm folded into the GEMM (QKV and SILU; norm_mode 1 only in the
+  // decode orientation): the
   // weights already carry the norm weight w (W[n][k] * w[k], rounded to bf16
   // at load) and the GEMM reads the raw hidden state, so every output of
   // token m is scaled by 1 / sqrt(ss_m / norm_width + norm_eps) before bias,
@@ -71,9 +72,13 @@ struct EpiArgs {
   float norm_eps;
   const float* norm_partials;  // 16-byte aligned
   int norm_slots;               // a multiple of 4
-  // EPI_RESID_SQ (decode orientation): the warp holding output features
-  // [32 i, 32 i + 32) for token m writes sq_out[m * sq_ld + i] = sum of the
-  // squares of those features' stored (bf16) values
+  // EPI_RESID_SQ: sums of squares of the stored (bf16) outputs for the next
+  // RMSNorm, token-major with sq_ld slots per token.  Decode orientation: the
+  // warp holding output features [32 i, 32 i + 32) for token m writes slot i.
+  // Prefill orientation: the epilogue thread of token m writes, for output
+  // tile ib, slot 2 ib + (its half of the tile's 16-column units; slot
+  // 2 ib + 1 is zero when one thread covers the whole tile), so
+  // sq_ld = 2 x the tiles across the output features.
   float* sq_out;
   int sq_ld;
 };
@@ -212,8 +217,10 @@ size_t attn_decode_partial_floats(int head_dim);
 int attn_decode_stages(int head_dim, int rows);
 
 // small.cu
+// sq (may be null): each row's sum of squares at sq[row * 4], zeros at
+// sq[row * 4 + 1..3] (the [token][slot] form the GEMMs' folded RMSNorm reads)
 cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,
-                         const int32_t* ids, int M, int H, uint16_t* h, int* status,
+                         const int32_t* ids, int M, int H, uint16_t* h, float* sq, int* status,
                          cudaStream_t st);
 // w_loaded: w is a model weight written at load time (read before the
 // dependency wait); otherwise it is read after it

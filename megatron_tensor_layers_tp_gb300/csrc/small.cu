@@ -27,7 +27,7 @@ namespace tpk {
 // ---------------------------------------------------------------------------
 __global__ void embed_kernel(const uint16_t* __restrict__ table, int vocab, int vocab_per_rank,
                              int t, const int32_t* __restrict__ ids, int M, int H,
-                             uint16_t* __restrict__ h, int* status) {
+                             uint16_t* __restrict__ h, float* __restrict__ sq, int* status) {
   pdl_launch_dependents();
   pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -36,26 +36,54 @@ __global__ void embed_kernel(const uint16_t* __restrict__ table, int vocab, int 
   const int id = ids[warp];
   uint4* dst = reinterpret_cast<uint4*>(h + (int64_t)warp * H);
   const int nvec = H / 8;
+  float ss = 0.f;
   if (id < 0 || id >= vocab) {
     if (lane == 0) record_status(status, kStatusTokenRange);
     for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-    return;
+  } else {
+    const int owner = id / vocab_per_rank;          // the one rank whose lookup hits
+    const int local = id - owner * vocab_per_rank;  // row inside that rank's shard
+    const uint4* src = reinterpret_cast<const uint4*>(
+        table + ((int64_t)owner * vocab_per_rank + local) * H);
+    // kEmbedBatch 16-byte loads of a lane in flight together, then their stores
+    constexpr int kEmbedBatch = 8;
+    for (int i0 = lane; i0 < nvec; i0 += 32 * kEmbedBatch) {
+      uint4 v[kEmbedBatch];
+#pragma unroll
+      for (int k = 0; k < kEmbedBatch; ++k) {
+        const int i = i0 + 32 * k;
+        v[k] = i < nvec ? __ldg(&src[i]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kEmbedBatch; ++k) {
+        const int i = i0 + 32 * k;
+        if (i < nvec) dst[i] = v[k];
+        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+        }
+      }
+    }
   }
-  const int owner = id / vocab_per_rank;          // the one rank whose lookup hits
-  const int local = id - owner * vocab_per_rank;  // row inside that rank's shard
-  const uint4* src = reinterpret_cast<const uint4*>(
-      table + ((int64_t)owner * vocab_per_rank + local) * H);
-  for (int i = lane; i < nvec; i += 32) dst[i] = __ldg(&src[i]);
+  if (sq) {
+    // the row's sum of squares for the RMSNorm of the first layer, in the
+    // [token][4 slots] form the GEMMs read (slot 0, the rest zero)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane < 4) sq[(int64_t)warp * 4 + lane] = lane == 0 ? ss : 0.f;
+  }
 }
 
 cudaError_t launch_embed(const uint16_t* table, int vocab, int vocab_per_rank, int t,
-                         const int32_t* ids, int M, int H, uint16_t* h, int* status,
+                         const int32_t* ids, int M, int H, uint16_t* h, float* sq, int* status,
                          cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int blocks = (M + warps_per_block - 1) / warps_per_block;
   return launch_k(embed_kernel, dim3(blocks), dim3(warps_per_block * 32), 0, st, table, vocab,
-                  vocab_per_rank, t, ids, M, H, h, status);
+                  vocab_per_rank, t, ids, M, H, h, sq, status);
 }
 
 // ---------------------------------------------------------------------------

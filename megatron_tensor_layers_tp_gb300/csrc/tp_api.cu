@@ -310,6 +310,13 @@ struct WsLayout {
 // next RMSNorm (decode orientation): 4 per 128-row output tile
 int norm_slots(const tp_config_t& c) { return cdiv(c.hidden, 128) * 4; }
 
+// Sums of squares a producer can leave per token: the decode GEMMs'
+// norm_slots, two per output tile in the prefill orientation (at least
+// ceil(H / 128) tiles), or the embedding's four.
+int norm_sq_slots_max(const tp_config_t& c) {
+  return std::max(norm_slots(c), (2 * cdiv(c.hidden, kPrefillBNs[kNumPrefillBN - 1]) + 3) / 4 * 4);
+}
+
 size_t max_gemm_tiles(const tp_config_t& c, int M) {
   // upper bound over every GEMM of the model for M tokens
   const int H = c.hidden, d = c.head_dim, t = c.t;
@@ -345,7 +352,7 @@ WsLayout ws_layout(const tp_model* m, int M) {
   L.act = take((size_t)M * c.intermediate * 2);
   L.hs = take((size_t)M * c.hidden * 2);
   L.rank_partials = take((size_t)c.t * M * c.hidden * sizeof(float));
-  L.norm_sq = take((size_t)kSwapMaxTokens * norm_slots(c) * sizeof(float));  // [token][slot]
+  L.norm_sq = take((size_t)std::max(M, 1) * norm_sq_slots_max(c) * sizeof(float));  // [token][slot]
   L.total = off;
   return L;
 }
@@ -489,8 +496,8 @@ tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
     a.e.ld_res = H;
     a.e.bias = W.bias;  // once: the ranks are already summed in the accumulator
     a.e.bias_group_stride = 0;
-    a.e.sq_out = p.swap ? sq_out : nullptr;  // sums of squares for the next RMSNorm
-    a.e.sq_ld = norm_slots(c);
+    a.e.sq_out = sq_out;  // sums of squares for the next RMSNorm
+    a.e.sq_ld = p.swap ? norm_slots(c) : (2 * a.b_tiles + 3) / 4 * 4;  // a multiple of 4
     epi = a.e.sq_out ? EPI_RESID_SQ : EPI_RESID;
   } else {
     a.n_groups = t;
@@ -506,10 +513,14 @@ tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
   return TP_OK;
 }
 
+// sq_out: where the fused reduction leaves each token's sums of squares
+// for the next RMSNorm (or null); *sq_slots: how many per token it left
+// (0: none).
 tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, const uint16_t* x,
                   int64_t x_rank_stride, int64_t ldx, int M, const uint16_t* residual,
                   uint16_t* y, int fused, void* ws, const WsLayout& L, cudaStream_t st,
-                  float* sq_out = nullptr) {
+                  float* sq_out = nullptr, int* sq_slots = nullptr) {
+  if (sq_slots) *sq_slots = 0;
   if (M == 0) return TP_OK;
   const int H = W.rows, t = W.ranks;
   GemmArgs a;
@@ -519,6 +530,7 @@ tp_status run_row(const tp_model* m, const char* name, const ShardedLinear& W, c
   if (s != TP_OK) return s;
   float* rp = at<float>(ws, L.rank_partials);
   TP_CHECK_CUDA(launch(m, name, st, [&] { return launch_gemm(p.swap, epi, a, p.smem, st); }));
+  if (sq_slots && epi == EPI_RESID_SQ) *sq_slots = a.e.sq_ld;
   if (!fused) {
     TP_CHECK_CUDA(launch(m, "reduce_ranks", st, [&] {
       return launch_reduce_ranks(rp, (int64_t)M * H, t, M, H, W.bias, residual, y, st);
@@ -1001,18 +1013,24 @@ tp_status tp_row_linear_reduce(const tp_model* m, int32_t layer, int32_t which,
                  static_cast<cudaStream_t>(stream));
 }
 
+// The vocab-parallel lookup (counted as its all-reduce); sq (or null): each
+// row's sum of squares in the [token][4 slots] form for the next RMSNorm.
+static tp_status embed_rows(const tp_model* m, const int32_t* ids, int M, uint16_t* h, float* sq,
+                            cudaStream_t st) {
+  m->stats.allreduces++;
+  m->stats.allreduce_payload_bytes += (int64_t)M * m->cfg.hidden * 2;
+  return cuda_status(launch(m, "vocab_embed", st, [&] {
+    return launch_embed(m->embed, m->cfg.vocab, m->cfg.vocab_per_rank, m->cfg.t, ids, M,
+                        m->cfg.hidden, h, sq, m->status, st);
+  }));
+}
+
 tp_status tp_vocab_embed(const tp_model* m, const int32_t* ids, int32_t M, tp_bf16* h,
                          void* stream) {
   if (!m || M < 0) return TP_ERR_ARG;
   if (M == 0) return TP_OK;
   if (!m->embed || !ids || !h || !aligned16(h)) return TP_ERR_ARG;
-  m->stats.allreduces++;
-  m->stats.allreduce_payload_bytes += (int64_t)M * m->cfg.hidden * 2;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return cuda_status(launch(m, "vocab_embed", st, [&] {
-    return launch_embed(m->embed, m->cfg.vocab, m->cfg.vocab_per_rank, m->cfg.t, ids, M,
-                        m->cfg.hidden, h, m->status, st);
-  }));
+  return embed_rows(m, ids, M, h, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 static void count_gather(const tp_model* m, int S) {
@@ -1139,12 +1157,13 @@ static EpiArgs qkv_epi(const tp_model* m, const tp_batch_t* b, int M, uint16_t* 
   return e;
 }
 
-// h_sq: on entry, whether the sums of squares of h's rows sit in the
-// workspace (the previous layer's down_proj left them); on exit, whether this
-// layer's down_proj left them for the next.
+// h_sq: on entry, how many partial sums of squares per token of h's rows sit
+// in the workspace (left by the previous layer's down_proj or by the
+// embedding; 0: none); on exit, how many this layer's down_proj left for the
+// next.
 static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b, uint16_t* h,
                                int fused, void* ws, const WsLayout& L, cudaStream_t st,
-                               bool* h_sq) {
+                               int* h_sq) {
   const tp_config_t& c = m->cfg;
   const LayerShards& Ls = m->layers[layer];
   const int M = b->n_tokens, H = c.hidden, d = c.head_dim;
@@ -1158,29 +1177,30 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   if (!kc || !vc || !aligned16(kc) || !aligned16(vc)) return TP_ERR_ARG;
   tp_status s;
   // Each RMSNorm's weight is folded into the GEMM after it (qkv_folded,
-  // gate_up_folded).  In the decode orientation that GEMM reads h itself and
-  // scales each token's outputs by its 1/rms, which its epilogue warps get
-  // while the weights stream:
-  //  - up to kNormInGemmTokens tokens by reading h's rows (every CTA reads
-  //    all M rows from L2);
-  //  - above that from the sums of squares the fused row-parallel GEMM that
-  //    wrote h left in the workspace (measured: a ~1 us loss at 16 tokens
-  //    from the extra epilogue work in o_proj / down_proj, a gain at 64);
-  //  - otherwise (the layer's first norm without such sums, the unfused
-  //    reduction) u = h / rms(h) runs first.
+  // gate_up_folded).  That GEMM reads h itself and scales each token's
+  // outputs by its 1/rms, which its epilogue gets
+  //  - in the decode orientation up to kNormInGemmTokens tokens by reading
+  //    h's rows while the weights stream (every CTA reads all M rows from L2);
+  //  - otherwise from the partial sums of squares that the fused row-parallel
+  //    GEMM (or the embedding) that wrote h left in the workspace (decode
+  //    orientation measured: a ~1 us loss at 16 tokens from the extra epilogue
+  //    work in o_proj / down_proj, a gain at 64; prefill orientation: two norm
+  //    kernels of ~10 us each fewer per layer);
+  //  - where neither applies (the layer's first norm without such sums, the
+  //    unfused reduction) u = h / rms(h) runs first.
   const bool swap = plan_gemm(M).swap;
-  const bool leaves_sq = swap && fused != 0 && M > kNormInGemmTokens;  // o_proj, down_proj
+  const bool leaves_sq = fused != 0 && (!swap || M > kNormInGemmTokens);  // o_proj, down_proj
   float* sq = at<float>(ws, L.norm_sq);
-  auto norm_in = [&](EpiArgs& e_, bool have_sq, const uint16_t** xin) -> tp_status {
+  auto norm_in = [&](EpiArgs& e_, int have_sq, const uint16_t** xin) -> tp_status {
     e_.norm_src = h;
     e_.norm_ld = H;
     e_.norm_width = H;
     e_.norm_eps = c.rms_eps;
     e_.norm_partials = sq;
-    e_.norm_slots = norm_slots(c);
+    e_.norm_slots = have_sq;
     *xin = h;
     if (swap && M <= kNormInGemmTokens) { e_.norm_mode = 1; return TP_OK; }
-    if (swap && have_sq) { e_.norm_mode = 2; return TP_OK; }
+    if (have_sq > 0) { e_.norm_mode = 2; return TP_OK; }
     e_.norm_mode = 0;
     *xin = u;
     return cuda_status(launch(m, "rmsnorm", st, [&] {
@@ -1249,8 +1269,9 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
     TP_CHECK_CUDA(launch(m, "attn_prefill", st, [&] { return launch_attn_prefill(a, nqb, st); }));
   }
   // o_proj (row-parallel) + reduction ① + residual
+  int o_sq = 0;
   if ((s = run_row(m, "gemm_o", Ls.o, o, c.q_heads_per_rank * d, nhd, M, h, h, fused, ws, L, st,
-                   leaves_sq ? sq : nullptr)) != TP_OK)
+                   leaves_sq ? sq : nullptr, &o_sq)) != TP_OK)
     return s;
   // DP attention: every group's hidden rows are gathered for the MLP (one
   // buffer here; counted as each rank receiving the other groups' rows)
@@ -1260,16 +1281,15 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
   }
   // RMSNorm(h) folded as above; gate_up (column-parallel) + SiLU(gate) * up
   EpiArgs e2 = base_epi(m, M);
-  if ((s = norm_in(e2, leaves_sq, &xin)) != TP_OK) return s;
+  if ((s = norm_in(e2, o_sq, &xin)) != TP_OK) return s;
   e2.out = act;
   e2.ld_out = c.intermediate;
   if ((s = run_column(m, "gemm_gate_up", Ls.gate_up_folded, xin, H, M, EPI_SILU, e2, ws, L, st)) !=
       TP_OK)
     return s;
   // down_proj (row-parallel) + reduction ② + residual
-  *h_sq = leaves_sq;
   return run_row(m, "gemm_down", Ls.down, act, c.inter_per_rank, c.intermediate, M, h, h, fused, ws,
-                 L, st, leaves_sq ? sq : nullptr);
+                 L, st, leaves_sq ? sq : nullptr, h_sq);
 }
 
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
@@ -1279,7 +1299,7 @@ tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b
   tp_status s = check_batch(m, b);
   if (s != TP_OK) return s;
   if (!ws_ok(m, b->n_tokens, ws, ws_bytes)) return TP_ERR_WORKSPACE;
-  bool h_sq = false;  // the caller's h comes without sums of squares
+  int h_sq = 0;  // the caller's h comes without sums of squares
   return layer_forward(m, layer, b, h_inout, fused, ws, ws_layout(m, b->n_tokens),
                        static_cast<cudaStream_t>(stream), &h_sq);
 }
@@ -1316,7 +1336,7 @@ tp_status tp_layer_forward_host(const tp_model* m, int32_t layer, const tp_batch
   } else {
     TP_CHECK_CUDA(cudaMemcpyAsync(h_dev, h_in_host, bytes, cudaMemcpyHostToDevice, st));
   }
-  bool h_sq = false;
+  int h_sq = 0;
   if ((s = layer_forward(m, layer, b, h_dev, fused, ws, ws_layout(m, b->n_tokens), st, &h_sq)) !=
       TP_OK)
     return s;
@@ -1345,8 +1365,13 @@ static tp_status stage_forward(const tp_model* m, int first, int n, const int32_
   if (!ws_ok(m, rows, ws, ws_bytes)) return TP_ERR_WORKSPACE;
   const WsLayout L = ws_layout(m, rows);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (ids && (s = tp_vocab_embed(m, ids, M, h, stream)) != TP_OK) return s;
-  bool h_sq = false;  // the stage's input h comes without sums of squares
+  // the embedding leaves each row's sum of squares for the first layer's
+  // RMSNorm (four slots per token); a stage's input h comes without them
+  int h_sq = 0;
+  if (ids) {
+    if ((s = embed_rows(m, ids, M, h, at<float>(ws, L.norm_sq), st)) != TP_OK) return s;
+    h_sq = 4;
+  }
   for (int l = first; l < first + n; ++l)
     if ((s = layer_forward(m, l, b, h, fused, ws, L, st, &h_sq)) != TP_OK) return s;
   if (!logits) return TP_OK;

@@ -149,13 +149,15 @@ def test_short_prefill_with_norm_inside_the_gemms_matches_oracle(t):
 
 
 @pytest.mark.parametrize("fused", [True, False])
-def test_norm_paths_above_32_tokens(fused):
-    # 48 tokens: the first RMSNorm runs as a kernel (unit weight: its weight is
-    # folded into qkv); with the fused reduction o_proj leaves the sums of
-    # squares of h and gate_up applies the second norm itself, with the
-    # unfused one (per-rank partials + reduction kernel) it is a kernel too
-    w = _wl("prefill", n_seqs=3, seq_len=16, ctx=16)
-    err, launches = _ragged_prefill(w, 2, [16, 16, 16], 7, fused=fused)
+@pytest.mark.parametrize("lens,pairs", [([16, 16, 16], 0), ([30, 50, 60], 1), ([30, 50, 60], 2)])
+def test_norm_paths_above_32_tokens(fused, lens, pairs):
+    # 48 tokens (decode orientation) or 140 (prefill orientation, CTA pairs or
+    # single CTAs): the first RMSNorm runs as a kernel (unit weight: its
+    # weight is folded into qkv); with the fused reduction o_proj leaves the
+    # sums of squares of h and gate_up applies the second norm itself, with
+    # the unfused one (per-rank partials + reduction kernel) it is a kernel too
+    w = _wl("prefill", n_seqs=3, seq_len=max(lens), ctx=max(lens))
+    err, launches = _ragged_prefill(w, 2, lens, 7, fused=fused, prefill_cta_pairs=pairs)
     assert err <= LAYER_TOL
     assert launches == (6 if fused else 9)
 
@@ -259,9 +261,9 @@ def test_two_layer_forward_with_padded_vocab_and_counters():
 @pytest.mark.parametrize("n_seqs,fused", [(6, True), (48, True), (48, False)])
 def test_three_layer_forward_norm_paths_match_oracle(n_seqs, fused):
     # 6 tokens: every RMSNorm inside qkv / gate_up, from h's rows.  48
-    # tokens, fused: one norm kernel (layer 0's first), the rest inside the
-    # GEMMs from the sums of squares the fused row-parallel GEMMs leave.  48
-    # unfused: every norm a kernel.
+    # tokens, fused: every norm inside the GEMMs, from the sums of squares the
+    # embedding (layer 0's first norm) and the fused row-parallel GEMMs leave.
+    # 48 unfused: every norm a kernel but layer 0's first.
     w = _wl("decode", n_seqs=n_seqs, seq_len=1, ctx=40, vocab=1001, layers=3, embed=True)
     t = 4
     model, _, _ = build_model(w, t)
@@ -273,8 +275,34 @@ def test_three_layer_forward_norm_paths_match_oracle(n_seqs, fused):
     torch.cuda.synchronize()
     assert model.check_device() == 0
     per_layer = 5 if fused else 7  # qkv, attention, o_proj, gate_up, down (+2 reductions)
-    norms = 0 if n_seqs <= 32 else (1 if fused else 6)
+    norms = 0 if n_seqs <= 32 or fused else 5
     assert model.stats().kernel_launches == 1 + 3 * per_layer + norms + 2  # embed ... head
+    ref = oracle_forward(w, ids_np)
+    assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
+    model.close()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("pairs", [1, 2])
+def test_three_layer_prefill_forward_norm_paths_match_oracle(fused, pairs):
+    # 2 x 80 tokens (the prefill orientation), on CTA pairs or single CTAs.
+    # Fused: every RMSNorm inside qkv / gate_up, scaled by the 1/rms from the
+    # sums of squares the embedding and the fused row-parallel GEMMs leave
+    # (per output tile of the prefill orientation); unfused: every norm but
+    # layer 0's first a kernel.
+    w = _wl("prefill", n_seqs=2, seq_len=80, ctx=80, vocab=1001, layers=3, embed=True)
+    t = 2
+    model, _, _ = build_model(w, t, prefill_cta_pairs=pairs)
+    batch, _ = make_batch(model, w)
+    ids_np = synth.token_ids(w)
+    ids = torch.from_numpy(ids_np).cuda()
+    model.reset_stats()
+    logits = model.forward(ids, batch, fused=fused)
+    torch.cuda.synchronize()
+    assert model.check_device() == 0
+    per_layer = 5 if fused else 7
+    norms = 0 if fused else 5
+    assert model.stats().kernel_launches == 1 + 3 * per_layer + norms + 2
     ref = oracle_forward(w, ids_np)
     assert rel_err(to_f64(logits), ref) <= LOGIT_TOL
     model.close()
