@@ -187,6 +187,13 @@ __global__ void __launch_bounds__(kPairThreads<EPI>, 1)
     const int row = quad * 32 + lane;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
     const int* tok = nullptr;  // token tables live in EpiArgs in this orientation
+    // the folded norm's 1/rms of this thread's row in the last two 256-row
+    // blocks seen: a pair's tiles p, p + P, ... revisit few row blocks (two
+    // when P is a multiple of half the row-block count), so the row's sums are
+    // read once per block rather than once per tile
+    int rs_blk0 = -1, rs_blk1 = -1;
+    float rs_val0 = 1.f, rs_val1 = 1.f;
+    bool rs_next1 = false;
     uint32_t seg = 0;
     for (int64_t tile = pair; tile < n_tiles; tile += P) {
       int g, ia, ib;
@@ -203,7 +210,19 @@ __global__ void __launch_bounds__(kPairThreads<EPI>, 1)
       // the token's 1/rms (folded norm) once per tile, its sum of squares over
       // this thread's units (EPI_RESID_SQ)
       float rs = 1.f, ss = 0.f;
-      if constexpr (kEpiNorm<EPI>) rs = prefill_row_rs(a.e, arow);
+      if constexpr (kEpiNorm<EPI>) {
+        const int blk = g * a.a_tiles + ia;
+        if (rs_blk0 == blk) {
+          rs = rs_val0;
+        } else if (rs_blk1 == blk) {
+          rs = rs_val1;
+        } else {
+          rs = prefill_row_rs(a.e, arow);
+          if (rs_next1) { rs_blk1 = blk; rs_val1 = rs; }
+          else { rs_blk0 = blk; rs_val0 = rs; }
+          rs_next1 = !rs_next1;
+        }
+      }
       EpiIn cur, nxt;
       const int c_first = half * 16;
       if (c_first < BN) epi_load<false, EPI>(a, g, arow, brow + c_first, tok, cur);
