@@ -283,13 +283,15 @@ typedef struct {
  *   h = h + all_reduce(row-parallel down_proj(a))        reduction ②
  * h_inout [n_tokens, H] bf16 is read and overwritten.  fused selects the
  * row-parallel reduction variant (see tp_row_linear_reduce).
- * Each RMSNorm's weight is folded into the GEMM after it (tp_load_shards).
- * Up to 32 tokens that GEMM reads h and scales token m's outputs by
- * 1/sqrt(mean(h_m^2) + eps), computed in fp32 inside it (five kernels per
- * layer).  Above 32 tokens (up to 64) the second norm takes its sums of
- * squares from o_proj (fused reduction), and in tp_forward / tp_stage_forward
- * so does every later layer's first norm (from down_proj); the first norm of
- * the call runs as a kernel. */
+ * Each RMSNorm's weight is folded into the GEMM after it (tp_load_shards):
+ * that GEMM reads h and scales token m's outputs by 1/sqrt(mean(h_m^2) +
+ * eps) in fp32.  Up to 32 tokens it computes mean(h_m^2) from h's rows (five
+ * kernels per layer).  Above that, with the fused reduction, the second norm
+ * takes partial sums of squares that o_proj leaves, and in tp_forward /
+ * tp_stage_forward so does every later layer's first norm (from down_proj)
+ * and the first layer's (from the embedding); the first norm of a
+ * tp_layer_forward call, and every norm with the unfused reduction, runs as a
+ * kernel.  The sums are added in a fixed order: the result is deterministic. */
 tp_status tp_layer_forward(const tp_model* m, int32_t layer, const tp_batch_t* b,
                            tp_bf16* h_inout, int32_t fused, void* ws, size_t ws_bytes,
                            void* stream);
