@@ -541,11 +541,8 @@ def run_ours(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded random-init weights ~N(0,0.02), KV cache ~N(0,1), hidden ~N(0,1)",
         "config": {
-            "workload": "Llama-3.1-8B-shaped decoder layer, decode: 16 sequences x 1 token, "
-                        "1024-token KV context, t emulated TP ranks on one GPU",
-            "hidden": w.hidden, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
-            "head_dim": w.head_dim, "intermediate": w.intermediate, "batch": w.n_seqs,
-            "ctx": w.ctx, "t": args.t, "fused_reduction": bool(args.fused),
+            **workload_config(w, args.t),
+            "fused_reduction": bool(args.fused),
             "parallelism": f"tp{args.t} emulated on 1 GPU" + (f", {world} replicas" if world > 1 else ""),
             "l2": f"inputs larger than L2: steps rotate over {args.rotate} layers with distinct "
                   f"weights and KV ({args.rotate * step_bytes / 1e9:.2f} GB)",
@@ -796,6 +793,15 @@ def oracle_step(w, t, inputs):
                                    O.Batch.decode(w.n_seqs, w.ctx), dims, p)
 
 
+def workload_config(w, t):
+    """The config keys both arms report for the decode-layer workload."""
+    return {"workload": "Llama-3.1-8B-shaped decoder layer, decode: 16 sequences x 1 token, "
+                        "1024-token KV context, t emulated TP ranks",
+            "hidden": w.hidden, "n_heads": w.n_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "intermediate": w.intermediate, "batch": w.n_seqs,
+            "ctx": w.ctx, "t": t}
+
+
 def cpu_baseline(w, t, budget_s):
     inputs = oracle_inputs(w)
     oracle_step(w, t, inputs)  # warm
@@ -834,8 +840,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "steps_run": n, "warmup": args.warmup,
         "ms_per_step": round(dt / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
-        "config": {"workload": "Llama-3.1-8B-shaped decoder layer, decode: 16 sequences x 1 token, "
-                               "1024-token KV context, t emulated TP ranks", "t": args.t},
+        "config": workload_config(w, args.t),
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} decode step(s) of {w.tokens} tokens (wall-time capped at "
