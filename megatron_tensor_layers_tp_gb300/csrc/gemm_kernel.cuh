@@ -17,15 +17,18 @@
 //    shared memory and are added in K order after a cluster barrier;
 //  - data-parallel waves of whole tiles (prefill orientation), the remainder
 //    as a last, partial wave of whole tiles.
-// The result is deterministic for a given grid.
+// The result is deterministic for a given grid.  (Prefill GEMMs with at least
+// one wave of 256-row tiles run on CTA pairs instead: gemm_pair.cuh, with the
+// epilogues defined here.)
 //
 // Roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma from one thread
 // into one of two TMEM accumulators, and the epilogue warps (eight in the
 // decode orientation, 320 threads; four in the prefill orientation, 192)
-// drain the other accumulator (tcgen05.ld) and run the epilogue.  In the
-// decode orientation the qkv and gate_up epilogue warps also work out each
-// token's 1/rms for the RMSNorm folded into those GEMMs while the weights
-// stream.  Every wait is bounded.
+// drain the other accumulator (tcgen05.ld) and run the epilogue.  The qkv and
+// gate_up epilogues also apply the RMSNorm folded into those GEMMs: each
+// token's 1/rms from h's rows (decode orientation, worked out by the epilogue
+// warps while the weights stream) or from the sums of squares the kernel
+// that wrote h left.  Every wait is bounded.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>

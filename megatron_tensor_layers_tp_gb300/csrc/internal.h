@@ -19,8 +19,8 @@ enum Epi : int {
   EPI_RESID = 3,    // fused row-parallel: y = residual + sum of rank partials
   EPI_PARTIAL = 4,  // unfused row-parallel: fp32 partial of each rank
   EPI_LOGITS = 5,   // LM head: logits placed in the rank's vocab slot
-  EPI_RESID_SQ = 6, // EPI_RESID (decode orientation) that also leaves the next
-                    // RMSNorm's sums of squares (EpiArgs::sq_out)
+  EPI_RESID_SQ = 6, // EPI_RESID that also leaves the next RMSNorm's partial
+                    // sums of squares (EpiArgs::sq_out; both orientations)
   EPI_QKV_PIECES = 7,  // qkv in the decode orientation, stream-K: every CTA only
                        // stores its fp32 pieces; the decode attention kernel sums
                        // them and finishes the qkv epilogue (norm, bias, RoPE, cache)
