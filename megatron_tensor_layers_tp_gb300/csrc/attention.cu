@@ -274,7 +274,8 @@ __device__ __forceinline__ float new_key_score(const uint8_t* sQ, int qrow_bytes
 }
 
 
-template <int D>
+// TQ: at most 8 query rows per KV head, taken on the MMA N side (attn_tile_t)
+template <int D, bool TQ>
 __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   using L = DecSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -405,12 +406,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         qkv_from_pieces<D>(a, b, g, pos, rs, writer, sQ, L::kQRow, knew, vnew);
         bar_sync(1, kDecWarps * 32);
       }
-      uint32_t qa[D / 16][4];
-      load_q_frags<D>(smem_u32(sQ), L::kQRow, qa);
+      // Q fragments: A of 16 query rows, or (TQ) B of Q^T over 8 query rows
+      constexpr int QR = TQ ? 2 : 4;   // registers per 16-wide d step
+      constexpr int ON = TQ ? D / 16 : D / 8;  // accumulator fragments
+      uint32_t qa[D / 16][QR];
+      if constexpr (TQ) load_qt_frags<D>(smem_u32(sQ), L::kQRow, qa);
+      else load_q_frags<D>(smem_u32(sQ), L::kQRow, qa);
       float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-      float o[D / 8][4];
+      float o[ON][4];
 #pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt)
+      for (int nt = 0; nt < ON; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
       // with the deferred qkv the new key is merged at the end, not read from the cache
@@ -431,34 +436,65 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         const int key0 = (tile0 + i) * kKeyTile + wq * kWarpKeys;
         if (key0 <= last_key) {
           const uint32_t st = smem_u32(tiles + s * L::kStageBytes);
-          attn_tile<D, kWarpKeys / 8>(qa, st, st + L::kTileBytes, wq * kWarpKeys, key0, lim,
-                                      a.scale_log2, m, l, o);
+          if constexpr (TQ) {
+            static_assert(kWarpKeys == 16, "one 16-key step per warp and tile");
+            attn_tile_t<D>(qa, st, st + L::kTileBytes, wq * kWarpKeys, key0, last_key,
+                           a.scale_log2, m, l, o);
+          } else {
+            attn_tile<D, kWarpKeys / 8>(qa, st, st + L::kTileBytes, wq * kWarpKeys, key0, lim,
+                                        a.scale_log2, m, l, o);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       n_base += len;
+      // each query row's l: the row's threads hold shares of it (TQ: the 8
+      // lanes of a column; otherwise the 4 lanes of a row)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+        if constexpr (TQ) {
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 4);
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+        } else {
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+        }
       }
       // combine: every warp's (m, l, O) meets the others in smem
       // (only the KV head's query rows: rows >= group hold no query)
       constexpr int CL = L::kCombLd;
       const int GR = a.group;
       float* cw = comb + warp * GR * CL;
-      const int r0 = lane >> 2;
+      if constexpr (TQ) {
+        // o[dt]: O^T rows (features) 16 dt + lane/4 and + 8, query columns
+        // 2 (lane % 4) and + 1
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int r = r0 + hh * 8;
-        if (r >= GR) continue;
+        for (int c = 0; c < 2; ++c) {
+          const int q = (lane & 3) * 2 + c;
+          if (q >= GR) continue;
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          const int col = nt * 8 + (lane & 3) * 2;
-          *reinterpret_cast<float2*>(cw + r * CL + col) = make_float2(o[nt][hh * 2], o[nt][hh * 2 + 1]);
+          for (int dt = 0; dt < D / 16; ++dt) {
+            cw[q * CL + dt * 16 + (lane >> 2)] = o[dt][c];
+            cw[q * CL + dt * 16 + 8 + (lane >> 2)] = o[dt][2 + c];
+          }
+          if ((lane >> 2) == 0) { cw[q * CL + D] = m[c]; cw[q * CL + D + 1] = l[c]; }
         }
-        if ((lane & 3) == 0) { cw[r * CL + D] = m[hh]; cw[r * CL + D + 1] = l[hh]; }
+      } else {
+        const int r0 = lane >> 2;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = r0 + hh * 8;
+          if (r >= GR) continue;
+#pragma unroll
+          for (int nt = 0; nt < D / 8; ++nt) {
+            const int col = nt * 8 + (lane & 3) * 2;
+            *reinterpret_cast<float2*>(cw + r * CL + col) =
+                make_float2(o[nt][hh * 2], o[nt][hh * 2 + 1]);
+          }
+          if ((lane & 3) == 0) { cw[r * CL + D] = m[hh]; cw[r * CL + D + 1] = l[hh]; }
+        }
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
       // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128): columns
@@ -697,17 +733,23 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
 // ============================================================================
 // host launchers
 // ============================================================================
-template <int D>
-static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
+template <int D, bool TQ>
+static cudaError_t launch_decode_tq(const AttnArgs& a, cudaStream_t st) {
   const size_t smem = DecSmem<D>::bytes(a.stages, a.group);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, TQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_k(attn_decode_kernel<D>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
+  return launch_k(attn_decode_kernel<D, TQ>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
+}
+
+// up to 8 query rows per KV head: query rows on the MMA N side
+template <int D>
+static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
+  return a.group <= 8 ? launch_decode_tq<D, true>(a, st) : launch_decode_tq<D, false>(a, st);
 }
 
 // The most K/V stages (even, at most DecSmem::kMaxStages) whose shared memory

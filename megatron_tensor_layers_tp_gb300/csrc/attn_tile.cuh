@@ -134,6 +134,99 @@ __device__ __forceinline__ void attn_tile(const uint32_t (&qa)[D / 16][4], uint3
   }
 }
 
+// Decode with at most 8 query rows per KV head (one token per sequence): the
+// keys go on the MMA M side and the query rows on N (S^T = K Q^T, then
+// O^T += V^T P^T), so a 16-key step needs half the MMAs and exponentials of a
+// 16-row query tile.
+
+// Transposes the 8x8 b16 matrix held in the usual fragment layout (thread t:
+// row t/4, columns 2(t%4) and 2(t%4)+1).
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// B fragments of Q^T (16 d x 8 query rows) for every 16-wide d step, from 8
+// padded query rows in shared memory (rows past the KV head's group are zero).
+template <int D>
+__device__ __forceinline__ void load_qt_frags(uint32_t sQ, int row_bytes, uint32_t (&qb)[D / 16][2]) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 3, r = lane & 7;
+#pragma unroll
+  for (int k2 = 0; k2 < D / 32; ++k2)  // matrix j: d columns (4 k2 + j) * 8 ..
+    ldsm_x4(sQ + r * row_bytes + (k2 * 4 + j) * 16, qb[2 * k2][0], qb[2 * k2][1],
+            qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
+}
+
+// One warp: scores of 16 keys (rows krow0.. of the smem tile) against the 8
+// query columns, then the online-softmax update of each column's (m, l) and
+// of O^T.  key0: position of the first key; lim: last visible key position.
+// m[c], l[c]: query columns 2 (lane % 4) + c; l holds this thread's share
+// (its two keys per step), summed over the 8 lanes of a column at the end.
+// o[dt]: O^T rows 16 dt + lane / 4 (+ 8), the same two columns.
+template <int D>
+__device__ __forceinline__ void attn_tile_t(const uint32_t (&qb)[D / 16][2], uint32_t sK,
+                                            uint32_t sV, int krow0, int key0, int lim,
+                                            float scale_log2, float (&m)[2], float (&l)[2],
+                                            float (&o)[D / 16][4]) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 3, r = lane & 7;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    // A = K[16 keys][16 d]: matrices (keys 0-7 | 8-15) x (d 0-7 | 8-15)
+    uint32_t a[4];
+    ldsm_x4(sK + kv_off(krow0 + (j & 1) * 8 + r, kk * 2 + (j >> 1)), a[0], a[1], a[2], a[3]);
+    mma_16816(s, a, qb[kk][0], qb[kk][1]);
+  }
+  // s: keys lane/4 (s[0], s[1]) and lane/4 + 8 (s[2], s[3]); columns 2 (lane%4) + 0/1
+  const int k_lo = key0 + (lane >> 2), k_hi = k_lo + 8;
+  float v[4];
+  v[0] = k_lo <= lim ? s[0] * scale_log2 : -INFINITY;
+  v[1] = k_lo <= lim ? s[1] * scale_log2 : -INFINITY;
+  v[2] = k_hi <= lim ? s[2] * scale_log2 : -INFINITY;
+  v[3] = k_hi <= lim ? s[3] * scale_log2 : -INFINITY;
+  float t[2] = {fmaxf(v[0], v[2]), fmaxf(v[1], v[3])};
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    t[c] = fmaxf(t[c], __shfl_xor_sync(0xffffffffu, t[c], 4));
+    t[c] = fmaxf(t[c], __shfl_xor_sync(0xffffffffu, t[c], 8));
+    t[c] = fmaxf(t[c], __shfl_xor_sync(0xffffffffu, t[c], 16));
+  }
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    mnew[c] = fmaxf(m[c], t[c]);
+    alpha[c] = (mnew[c] == -INFINITY) ? 1.f : exp2f(m[c] - mnew[c]);
+    m[c] = mnew[c];
+    l[c] *= alpha[c];
+  }
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = i & 1;
+    p[i] = (mnew[c] == -INFINITY) ? 0.f : exp2f(v[i] - mnew[c]);
+  }
+  l[0] += p[0] + p[2];
+  l[1] += p[1] + p[3];
+#pragma unroll
+  for (int dt = 0; dt < D / 16; ++dt) {
+    o[dt][0] *= alpha[0]; o[dt][1] *= alpha[1];
+    o[dt][2] *= alpha[0]; o[dt][3] *= alpha[1];
+  }
+  // P^T (16 keys x 8 columns) as the B operand: transpose each 8x8 block
+  const uint32_t b0 = movm_trans(pack2(p[0], p[1]));
+  const uint32_t b1 = movm_trans(pack2(p[2], p[3]));
+#pragma unroll
+  for (int dt = 0; dt < D / 16; ++dt) {
+    // A = V^T[16 d][16 keys]: transposed loads of V (keys 0-7 | 8-15) x (d 0-7 | 8-15)
+    uint32_t a[4];
+    ldsm_x4_t(sV + kv_off(krow0 + (j >> 1) * 8 + r, dt * 2 + (j & 1)), a[0], a[1], a[2], a[3]);
+    mma_16816(o[dt], a, b0, b1);
+  }
+}
+
 // Loads the A fragments of 16 query rows from a padded smem block.
 template <int D>
 __device__ __forceinline__ void load_q_frags(uint32_t sQ, int row_bytes, uint32_t (&qa)[D / 16][4]) {

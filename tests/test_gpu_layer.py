@@ -71,6 +71,18 @@ def test_decode_layer_matches_oracle(t, n_kv, fused):
 
 
 @pytest.mark.parametrize("t", [1, 2, 4])
+@pytest.mark.parametrize("n_heads,n_kv", [(8, 1), (12, 1), (16, 1), (16, 2)])
+def test_decode_layer_query_groups_match_oracle(t, n_heads, n_kv):
+    # query rows per KV head: 8 (the largest taken on the MMA N side), 12 and
+    # 16 (16-row query tiles), 8 with two KV heads
+    w = _wl("decode", n_seqs=5, seq_len=1, ctx=150, n_heads=n_heads, n_kv=n_kv)
+    model, h, _ = _run_layer(w, t)
+    ref, _, _ = _oracle_layer(w)
+    assert rel_err(to_f64(h), ref) <= LAYER_TOL
+    model.close()
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
 @pytest.mark.parametrize("head_dim,n_heads,n_kv", [(64, 8, 2), (128, 4, 4)])
 def test_prefill_layer_matches_oracle(t, head_dim, n_heads, n_kv):
     w = _wl("prefill", n_seqs=3, seq_len=70, ctx=70, head_dim=head_dim, n_heads=n_heads, n_kv=n_kv)
