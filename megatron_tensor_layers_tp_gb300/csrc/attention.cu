@@ -164,7 +164,8 @@ __device__ void qkv_from_pieces(const AttnArgs& a, int b, int g, int pos, float 
   const int kv_local = g % kvr;
   const int n_items = (a.group + 2) * half;
   const bool pos_ok = pos >= 0 && pos < a.l_max;
-  // (32-bit piece arithmetic: the host keeps pc_total * pc_grid below 2^31)
+  // (32-bit piece arithmetic: the host keeps pc_total * pc_grid below 2^31;
+  // the divisions by pc_total, pc_grid and q_per_rank are multiply-shifts)
   const int T = static_cast<int>(a.pc_total), Gp = a.pc_grid, K = a.pc_k;
   const int64_t piece = (int64_t)a.pc_bn * 128;
   const float* pcb = a.pc + (int64_t)b * 128;
@@ -182,7 +183,7 @@ __device__ void qkv_from_pieces(const AttnArgs& a, int b, int g, int pos, float 
         hq[u] = itc / half;
         ii[u] = itc - hq[u] * half;
         const int j = g * a.group + hq[u];
-        r[u] = j / nq;
+        r[u] = static_cast<int>(fast_div(static_cast<uint32_t>(j), a.pc_div_q));
         lr[u] = (j - r[u] * nq) * D + 2 * ii[u];
       } else {
         kind[u] = itc < (a.group + 1) * half ? 1 : 2;
@@ -192,9 +193,11 @@ __device__ void qkv_from_pieces(const AttnArgs& a, int b, int g, int pos, float 
         lr[u] = (nq + (kind[u] == 2 ? kvr : 0) + kv_local) * D + 2 * ii[u];
       }
       const int ts = r[u] * a.pc_a_tiles + lr[u] / 128;
-      c0[u] = ((ts * K + 1) * Gp - 1) / T;                       // owner of the tile's first step
-      ns[u] = (((ts + 1) * K) * Gp - 1) / T - c0[u] + 1;          // pieces of the tile
-      sl0[u] = (c0[u] * T) / Gp == ts * K ? 0 : 1;                // slot of the first piece
+      // owner of the tile's first step, pieces of the tile, slot of the first piece
+      c0[u] = static_cast<int>(fast_div(static_cast<uint32_t>((ts * K + 1) * Gp - 1), a.pc_div_total));
+      ns[u] = static_cast<int>(fast_div(static_cast<uint32_t>(((ts + 1) * K) * Gp - 1), a.pc_div_total)) -
+              c0[u] + 1;
+      sl0[u] = static_cast<int>(fast_div(static_cast<uint32_t>(c0[u] * T), a.pc_div_grid)) == ts * K ? 0 : 1;
       const float* src = pcb + lr[u] % 128;
 #pragma unroll
       for (int q = 0; q < kMaxPieces; ++q)

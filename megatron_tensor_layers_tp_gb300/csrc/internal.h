@@ -26,6 +26,33 @@ enum Epi : int {
                        // them and finishes the qkv epilogue (norm, bias, RoPE, cache)
 };
 
+// Unsigned division by an invariant divisor d (1 <= d < 2^31) as a multiply-
+// high, a subtract and two shifts: the round-up method of Granlund and
+// Montgomery, "Division by invariant integers using multiplication" (1994),
+// in the form that is exact for every 32-bit dividend.  With l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1; then n / d = (((n - q) >> s1) + q) >> s2
+// with q = mulhi(m, n), s1 = min(l, 1), s2 = max(l - 1, 0).
+struct FastDiv {
+  uint32_t m, s1, s2;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 0 ? l - 1 : 0;
+  return f;
+}
+__host__ __device__ inline uint32_t fast_div(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+  const uint32_t q = __umulhi(f.m, n);
+#else
+  const uint32_t q = static_cast<uint32_t>((static_cast<uint64_t>(f.m) * n) >> 32);
+#endif
+  return (((n - q) >> f.s1) + q) >> f.s2;
+}
+
 struct EpiArgs {
   int M;                    // tokens
   void* out;                // bf16 (or fp32 for EPI_PARTIAL)
@@ -142,6 +169,7 @@ struct AttnArgs {
   const float* pc;            // pieces [pc_grid][2][pc_bn][128] fp32 (stream-K slots)
   int64_t pc_total;           // the GEMM's stream-K K steps
   int pc_grid, pc_k, pc_bn;   // its grid, K steps per tile, token tile width
+  FastDiv pc_div_total, pc_div_grid, pc_div_q;  // by pc_total, pc_grid, q_per_rank
   int pc_a_tiles;             // 128-row tiles per rank
   int nqkv_r;                 // qkv shard rows per rank
   int q_per_rank, kv_replicas;

@@ -1239,6 +1239,9 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
       a.pc_total = g.total_iters;
       a.pc_grid = g.grid;
       a.pc_k = g.k_slices * g.k_iters_slice;
+      a.pc_div_total = make_fastdiv(static_cast<uint32_t>(a.pc_total));
+      a.pc_div_grid = make_fastdiv(static_cast<uint32_t>(a.pc_grid));
+      a.pc_div_q = make_fastdiv(static_cast<uint32_t>(c.q_heads_per_rank));
       a.pc_bn = g.BN;
       a.pc_a_tiles = g.a_tiles;
       a.nqkv_r = Ls.qkv_folded.rows;
