@@ -277,8 +277,9 @@ __device__ __forceinline__ float new_key_score(const uint8_t* sQ, int qrow_bytes
 }
 
 
-// TQ: at most 8 query rows per KV head, taken on the MMA N side (attn_tile_t)
-template <int D, bool TQ>
+// TQ: at most 8 query rows per KV head, taken on the MMA N side (attn_tile_t).
+// N32: AttnArgs::idx32 (the schedule's divisions as multiply-shifts).
+template <int D, bool TQ, bool N32>
 __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   using L = DecSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -314,16 +315,34 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
   const int G = a.grid, c = blockIdx.x;
   const int64_t T = a.total_units;
   const int TB = a.tiles_per_bg;
-  const int64_t beg = range_begin(c, T, G), end = range_begin(c + 1, T, G);
+  // the schedule's divisions (by total_units T, the grid G, tiles_per_bg TB
+  // and n_kv): multiply-shifts when every index fits 32 bits
+  auto start_of = [&](int cc) -> int64_t {
+    if constexpr (N32) return fast_div(static_cast<uint32_t>(cc * T), a.div_grid);
+    return range_begin(cc, T, G);
+  };
+  auto owner = [&](int64_t x) -> int {
+    if constexpr (N32) return static_cast<int>(fast_div(static_cast<uint32_t>((x + 1) * G - 1), a.div_units));
+    return owner_of(x, T, G);
+  };
+  auto pair_of = [&](int64_t u) -> int64_t {
+    if constexpr (N32) return fast_div(static_cast<uint32_t>(u), a.div_tb);
+    return u / TB;
+  };
+  auto seq_of = [&](int64_t bg) -> int {
+    if constexpr (N32) return static_cast<int>(fast_div(static_cast<uint32_t>(bg), a.div_kv));
+    return static_cast<int>(bg / a.n_kv);
+  };
+  const int64_t beg = start_of(c), end = start_of(c + 1);
 
   if (warp == kDecWarps) {
     // producer
     if (lane == 0) {
       uint32_t n = 0;
       // (sequence, KV head, tile) of unit u, walked incrementally
-      const int64_t bg0 = beg / TB;
+      const int64_t bg0 = pair_of(beg);
       int tile = static_cast<int>(beg - bg0 * TB);
-      int b = static_cast<int>(bg0 / a.n_kv), g = static_cast<int>(bg0 % a.n_kv);
+      int b = seq_of(bg0), g = static_cast<int>(bg0 - (int64_t)b * a.n_kv);
       auto issue = [&](uint32_t s) {
         const int slice = ((g / a.kv_r) * a.n_seqs + b) * a.kv_r + (g % a.kv_r);
         mbar_arrive_expect_tx(&full[s], L::kStageBytes);
@@ -376,7 +395,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
     int first_pos = 0;
     float first_rs = 1.f;
     if (beg < end) {
-      const int b0 = static_cast<int>((beg / TB) / a.n_kv);
+      const int b0 = seq_of(pair_of(beg));
       first_pos = a.positions[b0];
       if (a.qkv_pieces) first_rs = token_rs<D>(a, b0, red);
     }
@@ -384,11 +403,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
     uint32_t n_base = 0;           // CTA-local index of the segment's first unit
     bool alive = true;
     for (int64_t u0 = beg; u0 < end;) {
-      const int64_t bg = u0 / TB;
+      const int64_t bg = pair_of(u0);
       const int64_t seg_end = min(end, (bg + 1) * TB);
       const int len = static_cast<int>(seg_end - u0);
       const int tile0 = static_cast<int>(u0 - bg * TB);
-      const int b = static_cast<int>(bg / a.n_kv), g = static_cast<int>(bg % a.n_kv);
+      const int b = seq_of(bg), g = static_cast<int>(bg - (int64_t)b * a.n_kv);
       const bool first_seg = u0 == beg;
       const int pos = first_seg ? first_pos : a.positions[b];
       // stage the group's query rows (16 rows, zero beyond the group)
@@ -404,7 +423,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
       if (a.qkv_pieces) {
         // q, and the new token's k and v, from the qkv GEMM's pieces; the
         // pair's first CTA stores the new K/V row in the cache
-        const bool writer = owner_of(bg * TB, T, G) == c;
+        const bool writer = owner(bg * TB) == c;
         const float rs = first_seg ? first_rs : token_rs<D>(a, b, red);
         qkv_from_pieces<D>(a, b, g, pos, rs, writer, sQ, L::kQRow, knew, vnew);
         bar_sync(1, kDecWarps * 32);
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
 #pragma unroll
         for (int j = 0; j < CPT; ++j) acc[j] += cr[cl + 16 * j] * sc;
       }
-      const int nseg = owner_of((bg + 1) * TB - 1, T, G) - owner_of(bg * TB, T, G) + 1;
+      const int nseg = owner((bg + 1) * TB - 1) - owner(bg * TB) + 1;
       uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
       // the new key's state (score s_new, weight 1, value vnew) joins the
       // pair's final combination
@@ -540,8 +559,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         if (a.qkv_pieces) add_new_key(mm, ll, acc);
         if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
       } else {
-        const int first_c = owner_of(bg * TB, T, G);
-        const int my_slot = (beg / TB == bg) ? 0 : 1;
+        const int first_c = owner(bg * TB);
+        const int my_slot = (pair_of(beg) == bg) ? 0 : 1;
         float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
 #pragma unroll
         for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + cl + 16 * j] = acc[j];
@@ -560,7 +579,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
           float M2 = -INFINITY;
           for (int sgi = 0; sgi < nseg; ++sgi) {
             const int cc = first_c + sgi;
-            const int slot = (range_begin(cc, T, G) / TB == bg) ? 0 : 1;
+            const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
             const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
             M2 = fmaxf(M2, __ldcg(&src[row * (D + 2) + D]));
           }
@@ -569,7 +588,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
           for (int j = 0; j < CPT; ++j) acc2[j] = 0.f;
           for (int sgi = 0; sgi < nseg; ++sgi) {
             const int cc = first_c + sgi;
-            const int slot = (range_begin(cc, T, G) / TB == bg) ? 0 : 1;
+            const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
             const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
             const float ms = __ldcg(&src[row * (D + 2) + D]);
             if (ms == -INFINITY) continue;
@@ -736,23 +755,25 @@ __global__ void __launch_bounds__(kPreThreads) attn_prefill_kernel(const __grid_
 // ============================================================================
 // host launchers
 // ============================================================================
-template <int D, bool TQ>
+template <int D, bool TQ, bool N32>
 static cudaError_t launch_decode_tq(const AttnArgs& a, cudaStream_t st) {
   const size_t smem = DecSmem<D>::bytes(a.stages, a.group);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, TQ>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, TQ, N32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_k(attn_decode_kernel<D, TQ>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
+  return launch_k(attn_decode_kernel<D, TQ, N32>, dim3(a.grid), dim3(kDecThreads), smem, st, a);
 }
 
 // up to 8 query rows per KV head: query rows on the MMA N side
 template <int D>
 static cudaError_t launch_decode_t(const AttnArgs& a, cudaStream_t st) {
-  return a.group <= 8 ? launch_decode_tq<D, true>(a, st) : launch_decode_tq<D, false>(a, st);
+  if (a.idx32)
+    return a.group <= 8 ? launch_decode_tq<D, true, true>(a, st) : launch_decode_tq<D, false, true>(a, st);
+  return a.group <= 8 ? launch_decode_tq<D, true, false>(a, st) : launch_decode_tq<D, false, false>(a, st);
 }
 
 // The most K/V stages (even, at most DecSmem::kMaxStages) whose shared memory

@@ -156,6 +156,10 @@ struct AttnArgs {
   int tiles_per_bg;
   int64_t total_units;
   int grid;
+  // total_units * grid < 2^31: the schedule's divisions by total_units, grid,
+  // tiles_per_bg and n_kv are multiply-shifts (else 64-bit divisions)
+  int idx32;
+  FastDiv div_units, div_grid, div_tb, div_kv;
   int stages;                 // K/V stages in shared memory (even)
   float* partials;            // [grid][2][16][d+2]
   int* tickets;               // [n_seqs*n_kv]

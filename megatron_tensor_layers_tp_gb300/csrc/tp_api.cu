@@ -1130,6 +1130,13 @@ static tp_status prep_attention(const tp_model* m, const tp_batch_t* b, uint16_t
       }
     }
     a.grid = grid;
+    a.idx32 = a.total_units * grid < ((int64_t)1 << 31) ? 1 : 0;
+    if (a.idx32) {
+      a.div_units = make_fastdiv(static_cast<uint32_t>(a.total_units));
+      a.div_grid = make_fastdiv(static_cast<uint32_t>(grid));
+      a.div_tb = make_fastdiv(static_cast<uint32_t>(a.tiles_per_bg));
+      a.div_kv = make_fastdiv(static_cast<uint32_t>(c.n_kv_heads));
+    }
     a.stages = attn_decode_stages(d, a.group);
     if (a.stages < 2) return TP_ERR_UNSUPPORTED;
     a.partials = at<float>(ws, L.attn_partials);
