@@ -869,13 +869,27 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
         ++seg;
         continue;
       }
-      // pieces of this tile in the stream-K part (1 for a data-parallel tile)
+      // pieces of this tile in the stream-K part (1 for a data-parallel tile);
+      // with fix32 the divisions are multiply-shifts (they sit on the tail)
+      auto owner_fx = [&](int64_t x) -> int {
+        if (a.fix32)
+          return static_cast<int>(fast_div(static_cast<uint32_t>((x + 1) * Gs - 1), a.div_total));
+        return owner_of(x, T, Gs);
+      };
+      auto start_fx = [&](int cc) -> int64_t {
+        if (a.fix32) return fast_div(static_cast<uint32_t>(cc * T), a.div_sk);
+        return range_begin(cc, T, Gs);
+      };
+      auto step_tile = [&](int64_t x) -> int64_t {
+        if (a.fix32) return fast_div(static_cast<uint32_t>(x), a.div_k);
+        return x / K;
+      };
       int nseg = 1, c_first = c;
       int64_t ts = 0;
       if (sg.sk) {
         ts = sg.tile - dp_tiles;
-        c_first = owner_of(ts * K, T, Gs);
-        nseg = owner_of((ts + 1) * K - 1, T, Gs) - c_first + 1;
+        c_first = owner_fx(ts * K);
+        nseg = owner_fx((ts + 1) * K - 1) - c_first + 1;
       }
       if (nseg == 1) {
         if constexpr (SWAP) {
@@ -913,7 +927,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
       } else {
         // my piece of the tile -> workspace slot 0 (tile where my range starts) or 1
-        const int my_slot = (beg / K == ts) ? 0 : 1;
+        const int my_slot = (step_tile(beg) == ts) ? 0 : 1;
         float* mine = a.partials + ((int64_t)(c * 2 + my_slot) * BN) * 128;
         for (int c0 = half * U; c0 < BN; c0 += NH * U) {
           float v[16];
@@ -945,7 +959,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
           // piece then sits in slot 1).  Loads of up to 4 pieces are in flight
           // together, and the first batch of the next chunk is fetched before
           // the current chunk is stored.
-          const int slot0 = range_begin(c_first, T, Gs) == ts * K ? 0 : 1;
+          const int slot0 = start_fx(c_first) == ts * K ? 0 : 1;
           const float* base = a.partials + (int64_t)c_first * 2 * BN * 128 + row;
           float tmp[4][16];
           auto load_batch = [&](int c0, int s0) {

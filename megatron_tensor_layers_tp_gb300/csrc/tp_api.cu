@@ -250,6 +250,20 @@ PrefillChoice choose_prefill(const tp_model* m, int epi, int64_t groups, int M, 
 // taking 1/s of K, pieces added in K order through distributed shared memory
 // (no global partials, no tail fix-up).  Used when the tiles x s CTAs cover at
 // least 80% of the SMs and all those clusters can be resident at once.
+// The stream-K fix-up's divisions as multiply-shifts when every flat index
+// times the grid fits 31 bits (after the schedule is set).
+void set_fix32(GemmArgs& a) {
+  const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
+  const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
+  const int Gs = a.sk_ctas > 0 ? a.sk_ctas : a.grid;
+  a.fix32 = a.total_iters > 0 && n_tiles * K * std::max(a.grid, 1) < ((int64_t)1 << 31) ? 1 : 0;
+  if (a.fix32) {
+    a.div_total = make_fastdiv(static_cast<uint32_t>(a.total_iters));
+    a.div_sk = make_fastdiv(static_cast<uint32_t>(Gs));
+    a.div_k = make_fastdiv(static_cast<uint32_t>(K));
+  }
+}
+
 void set_schedule(GemmArgs& a, const GemmPlan& p, int num_sms, int epi) {
   const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
@@ -421,6 +435,7 @@ tp_status prep_column(const tp_model* m, const ShardedLinear& W, const uint16_t*
   a.k_slices = 1;
   a.k_iters_slice = cdiv(K, 64);
   set_schedule(a, p, m->num_sms, epi);
+  set_fix32(a);
   a.partials = at<float>(ws, L.gemm_partials);
   a.tickets = at<int>(ws, L.gemm_tickets);
   a.status = m->status;
@@ -510,6 +525,7 @@ tp_status prep_row(const tp_model* m, const ShardedLinear& W, const uint16_t* x,
     epi = EPI_PARTIAL;
   }
   set_schedule(a, p, m->num_sms, epi);
+  set_fix32(a);
   return TP_OK;
 }
 
@@ -1235,6 +1251,7 @@ static tp_status layer_forward(const tp_model* m, int layer, const tp_batch_t* b
     g.sk_ctas = 0;
     g.total_iters = n_tiles * g.k_slices * g.k_iters_slice;
     g.grid = (int)std::min<int64_t>(m->num_sms, g.total_iters);
+    set_fix32(g);
     // every CTA's range spans at most two tiles when there are no more tiles
     // than CTAs; the attention kernel locates pieces in 32-bit arithmetic
     if (n_tiles <= g.grid && g.total_iters * g.grid < (int64_t)1 << 31) {
