@@ -517,6 +517,7 @@ struct SegIter {
   int64_t it;
   int split;   // cluster split-K: one segment, 1/split of tile c / split's K range
   bool used;
+  const FastDiv* dk;  // division by K as a multiply-shift (null: 64-bit division)
   __device__ __forceinline__ bool next(Segment& s) {
     if (split > 1) {
       if (used) return false;
@@ -537,7 +538,7 @@ struct SegIter {
       return true;
     }
     if (it >= end) return false;
-    const int64_t ts = it / K;
+    const int64_t ts = dk ? static_cast<int64_t>(fast_div(static_cast<uint32_t>(it), *dk)) : it / K;
     const int64_t seg_end = min(end, (ts + 1) * K);
     s.tile = dp_tiles + ts;
     s.k0 = static_cast<int>(it - ts * K);
@@ -592,15 +593,29 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
   const int Gs = a.sk_ctas > 0 ? a.sk_ctas : G;  // CTAs sharing the stream-K part
   const int64_t beg = c < Gs ? range_begin(c, T, Gs) : T;
   const int64_t end = c < Gs ? range_begin(c + 1, T, Gs) : T;
-  auto make_iter = [&]() {
+  // Index divisions: after the dependency wait (fast = true) they are
+  // multiply-shifts when the host set fix32; the weight loads issued before
+  // the wait keep 64-bit divisions (measured: speeding those up made the
+  // decode step slower, its first loads then competing with the tail of the
+  // kernel before)
+  auto make_iter = [&](bool fast) {
     SegIter si;
     si.G = G; si.c = c; si.K = K; si.W = a.dp_waves;
     si.dp_tiles = dp_tiles; si.T = T; si.beg = beg; si.end = end;
     si.w = 0; si.it = beg;
     si.split = a.cluster_split; si.used = false;
+    si.dk = fast && a.fix32 ? &a.div_k : nullptr;
     return si;
   };
-  auto tile_coords = [&](int64_t tile, int& g, int& ia, int& ib) {
+  auto tile_coords = [&](int64_t tile, int& g, int& ia, int& ib, bool fast) {
+    if (fast && a.fix32) {
+      const uint32_t rest = fast_div(static_cast<uint32_t>(tile), a.div_a);
+      ia = static_cast<int>(static_cast<uint32_t>(tile) - rest * a.a_tiles);
+      const uint32_t gq = fast_div(rest, a.div_b);
+      ib = static_cast<int>(rest - gq * a.b_tiles);
+      g = static_cast<int>(gq);
+      return;
+    }
     ia = static_cast<int>(tile % a.a_tiles);
     const int64_t rest = tile / a.a_tiles;
     ib = static_cast<int>(rest % a.b_tiles);
@@ -649,11 +664,11 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       const int kis = a.k_iters_slice;
       uint32_t pre = 0;
       {
-        SegIter si = make_iter();
+        SegIter si = make_iter(false);
         Segment sg;
         while (pre < (uint32_t)S && si.next(sg)) {
           int g, ia, ib;
-          tile_coords(sg.tile, g, ia, ib);
+          tile_coords(sg.tile, g, ia, ib, false);
           int ks = sg.k0 / kis, kk = sg.k0 - ks * kis;
           for (int k = sg.k0; k < sg.k1 && pre < (uint32_t)S; ++k, ++pre) {
             mbar_arrive_expect_tx(&full[pre], kATileBytes + b_tile_bytes);
@@ -665,11 +680,11 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       pdl_wait();
       uint32_t n = 0, s = 0, ph = 0;  // load count, stage, stage phase
       bool ok = true;
-      SegIter si = make_iter();
+      SegIter si = make_iter(true);
       Segment sg;
       while (ok && si.next(sg)) {
         int g, ia, ib;
-        tile_coords(sg.tile, g, ia, ib);
+        tile_coords(sg.tile, g, ia, ib, true);
         int ks = sg.k0 / kis, kk = sg.k0 - ks * kis;
         for (int k = sg.k0; k < sg.k1; ++k, ++n) {
           if (n >= pre) {
@@ -694,7 +709,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       const uint32_t idesc = idesc_bf16_f32(128, BN);
       uint32_t seg = 0, s = 0, ph = 0;  // segment count, stage, stage phase
       bool ok = true;
-      SegIter si = make_iter();
+      SegIter si = make_iter(true);
       Segment sg;
       while (ok && si.next(sg)) {
         const uint32_t buf = seg & 1, use = seg >> 1;
@@ -805,23 +820,23 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
     const int ustep = NH * (a.cluster_split > 1 ? a.cluster_split : 1) * U;
     const int chunk0 = a.cluster_split > 1 ? u0 : half * U;
     {
-      SegIter t = make_iter();
+      SegIter t = make_iter(true);
       Segment last, x;
       while (t.next(x)) { last = x; ++n_segs; }
       if (SWAP && n_segs > 0 && chunk0 < BN) {
         int g, ia, ib;
-        tile_coords(last.tile, g, ia, ib);
+        tile_coords(last.tile, g, ia, ib, true);
         epi_load<SWAP, EPI>(a, g, ia * 128 + row, ib * BN + chunk0, tok, pre);
         pre_ok = true;
       }
     }
     uint32_t seg = 0;
-    SegIter si = make_iter();
+    SegIter si = make_iter(true);
     Segment sg;
     while (si.next(sg)) {
       const bool use_pre = pre_ok && (int)seg == n_segs - 1;
       int g, ia, ib;
-      tile_coords(sg.tile, g, ia, ib);
+      tile_coords(sg.tile, g, ia, ib, true);
       const uint32_t buf = seg & 1, use = seg >> 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&acc_full[buf], use & 1, a.status);
@@ -1026,7 +1041,7 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       const int row = (warp & 3) * 32 + lane;
       const int64_t tile = c / a.cluster_split;
       int g, ia, ib;
-      tile_coords(tile, g, ia, ib);
+      tile_coords(tile, g, ia, ib, true);
       const int arow = ia * 128 + row, brow = ib * BN;
       const uint32_t red_s = smem_u32(smem);
       // rank r sums and stores chunks r, r + s, ...; the pieces are added in

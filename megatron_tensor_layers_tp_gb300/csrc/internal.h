@@ -132,8 +132,10 @@ struct GemmArgs {
   int64_t total_iters;      // (n_tiles - W*G) * k_slices * k_iters_slice (stream-K part)
   int pair;                 // 1: prefill orientation on CTA pairs (gemm_pair_kernel): a_tiles
                             // counts 256-row tiles, tmB has a box of BN/2 rows, grid = 2 x pairs
-  int fix32;                // 1: the stream-K fix-up divides by multiply-shifts
+  int fix32;                // 1: every flat index x grid < 2^31: the index divisions after
+                            // the dependency wait are multiply-shifts
   FastDiv div_total, div_sk, div_k;  // by total_iters, the stream-K CTA count, K steps per tile
+  FastDiv div_a, div_b;              // by a_tiles, b_tiles
   int sk_ctas;              // CTAs 0..sk_ctas-1 share the stream-K part (0: all G); with
                             // sk_ctas = n_tiles - W*G each of them takes one whole tile
   float* partials;          // [G][2][BN][128]

@@ -256,11 +256,14 @@ void set_fix32(GemmArgs& a) {
   const int64_t n_tiles = (int64_t)a.n_groups * a.a_tiles * a.b_tiles;
   const int64_t K = (int64_t)a.k_slices * a.k_iters_slice;
   const int Gs = a.sk_ctas > 0 ? a.sk_ctas : a.grid;
-  a.fix32 = a.total_iters > 0 && n_tiles * K * std::max(a.grid, 1) < ((int64_t)1 << 31) ? 1 : 0;
+  a.fix32 = n_tiles * K * std::max(a.grid, 1) < ((int64_t)1 << 31) ? 1 : 0;
+  if (a.total_iters <= 0) a.fix32 = 0;  // no stream-K part: nothing to divide by
   if (a.fix32) {
     a.div_total = make_fastdiv(static_cast<uint32_t>(a.total_iters));
     a.div_sk = make_fastdiv(static_cast<uint32_t>(Gs));
     a.div_k = make_fastdiv(static_cast<uint32_t>(K));
+    a.div_a = make_fastdiv(static_cast<uint32_t>(a.a_tiles));
+    a.div_b = make_fastdiv(static_cast<uint32_t>(a.b_tiles));
   }
 }
 
