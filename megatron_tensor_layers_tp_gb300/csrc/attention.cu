@@ -519,87 +519,138 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         }
       }
       const bool any_dead = bar_sync_or(1, kDecWarps * 32, !alive);
-      // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128): columns
-      // cl, cl + 16, ... so that a row's 16 threads read 16 consecutive floats
-      constexpr int CPT = D / 16;
-      const int row = ctid >> 4, cl = ctid & 15;
-      const float s_new =
-          a.qkv_pieces ? new_key_score<D>(sQ, L::kQRow, knew, row, cl, a.scale_log2) : -INFINITY;
-      const int crow = row < GR ? row : 0;  // rows >= group: computed, never stored
-      float mm = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * GR + crow) * CL + D]);
-      float ll = 0.f, acc[CPT];
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
-#pragma unroll 2
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float* cr = comb + (w * GR + crow) * CL;
-        const float mw = cr[D];
-        if (mw == -INFINITY) continue;
-        const float sc = exp2f(mw - mm);
-        ll += cr[D + 1] * sc;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) acc[j] += cr[cl + 16 * j] * sc;
-      }
       const int nseg = owner((bg + 1) * TB - 1) - owner(bg * TB) + 1;
-      uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
-      // the new key's state (score s_new, weight 1, value vnew) joins the
-      // pair's final combination
-      auto add_new_key = [&](float& m_, float& l_, float (&o_)[CPT]) {
-        const float mn = fmaxf(m_, s_new);
-        const float so = m_ == -INFINITY ? 0.f : exp2f(m_ - mn);
-        const float sn = exp2f(s_new - mn);
-        l_ = l_ * so + sn;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) o_[j] = o_[j] * so + vnew[cl + 16 * j] * sn;
-        m_ = mn;
-      };
-      if (nseg == 1) {
-        if (a.qkv_pieces) add_new_key(mm, ll, acc);
-        if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
-      } else {
-        const int first_c = owner(bg * TB);
-        const int my_slot = (pair_of(beg) == bg) ? 0 : 1;
-        float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + cl + 16 * j] = acc[j];
-        if ((ctid & 15) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
-        // publish the record and take the pair's ticket: one thread fences
-        // for the CTA around the increment (the barriers carry the ordering)
-        bar_sync(1, kDecWarps * 32);
-        if (ctid == 0) {
-          fence_acq_rel_gpu();
-          const int old = atomicAdd(&a.tickets[bg], 1);
-          fence_acq_rel_gpu();
-          *last_flag = (old == nseg - 1) ? 1 : 0;
+      if (TQ && nseg == 1) {
+        // A whole pair with at most 8 query rows: all 256 threads on the real
+        // rows (64 threads per row for up to 4 rows, 32 for up to 8), 2-4
+        // columns each, instead of 16 threads on each of 16 rows.  The new
+        // key's score of each row comes first (16 threads per row).
+        if (a.qkv_pieces) {
+          const float sn = new_key_score<D>(sQ, L::kQRow, knew, ctid >> 4, ctid & 15, a.scale_log2);
+          if ((ctid & 15) == 0 && (ctid >> 4) < 8) red[ctid >> 4] = sn;
+          bar_sync(1, kDecWarps * 32);
         }
-        bar_sync(1, kDecWarps * 32);
-        if (*last_flag) {
-          float M2 = -INFINITY;
-          for (int sgi = 0; sgi < nseg; ++sgi) {
-            const int cc = first_c + sgi;
-            const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
-            const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
-            M2 = fmaxf(M2, __ldcg(&src[row * (D + 2) + D]));
-          }
-          float L2 = 0.f, acc2[CPT];
+        const int tpr = GR <= 4 ? (kDecWarps * 32) / 4 : (kDecWarps * 32) / 8;
+        const int row = ctid / tpr, cl = ctid % tpr;
+        constexpr int kMaxCpt = D / 32;  // columns per thread at 32 threads per row
+        const int cpt = D / tpr;
+        if (row < GR) {
+          float mm = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < CPT; ++j) acc2[j] = 0.f;
-          for (int sgi = 0; sgi < nseg; ++sgi) {
-            const int cc = first_c + sgi;
-            const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
-            const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
-            const float ms = __ldcg(&src[row * (D + 2) + D]);
-            if (ms == -INFINITY) continue;
-            const float sc = exp2f(ms - M2);
-            L2 += __ldcg(&src[row * (D + 2) + D + 1]) * sc;
+          for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * GR + row) * CL + D]);
+          float ll = 0.f, acc[kMaxCpt];
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + cl + 16 * j]) * sc;
+          for (int j = 0; j < kMaxCpt; ++j) acc[j] = 0.f;
+#pragma unroll
+          for (int w = 0; w < kDecWarps; ++w) {
+            const float* cr = comb + (w * GR + row) * CL;
+            const float mw = cr[D];
+            if (mw == -INFINITY) continue;
+            const float sc = exp2f(mw - mm);
+            ll += cr[D + 1] * sc;
+#pragma unroll
+            for (int j = 0; j < kMaxCpt; ++j)
+              if (j < cpt) acc[j] += cr[cl + tpr * j] * sc;
           }
-          if (a.qkv_pieces) add_new_key(M2, L2, acc2);
-          if (row < a.group) store_out_row<CPT>(orow, acc2, 1.f / L2);
-          if (ctid == 0) a.tickets[bg] = 0;
+          if (a.qkv_pieces) {
+            // the new key's state (score, weight 1, value vnew) joins in
+            const float s_new = red[row];
+            const float mn = fmaxf(mm, s_new);
+            const float so = mm == -INFINITY ? 0.f : exp2f(mm - mn);
+            const float sw = exp2f(s_new - mn);
+            ll = ll * so + sw;
+#pragma unroll
+            for (int j = 0; j < kMaxCpt; ++j)
+              if (j < cpt) acc[j] = acc[j] * so + vnew[cl + tpr * j] * sw;
+          }
+          const float inv = 1.f / ll;
+          uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
+#pragma unroll
+          for (int j = 0; j < kMaxCpt; ++j)
+            if (j < cpt) orow[tpr * j] = f_to_bf16(acc[j] * inv);
+        }
+      } else {
+        // 256 threads: row = ctid / 16, D/16 columns each (8 for D = 128): columns
+        // cl, cl + 16, ... so that a row's 16 threads read 16 consecutive floats
+        constexpr int CPT = D / 16;
+        const int row = ctid >> 4, cl = ctid & 15;
+        const float s_new =
+            a.qkv_pieces ? new_key_score<D>(sQ, L::kQRow, knew, row, cl, a.scale_log2) : -INFINITY;
+        const int crow = row < GR ? row : 0;  // rows >= group: computed, never stored
+        float mm = -INFINITY;
+  #pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, comb[(w * GR + crow) * CL + D]);
+        float ll = 0.f, acc[CPT];
+  #pragma unroll
+        for (int j = 0; j < CPT; ++j) acc[j] = 0.f;
+  #pragma unroll 2
+        for (int w = 0; w < kDecWarps; ++w) {
+          const float* cr = comb + (w * GR + crow) * CL;
+          const float mw = cr[D];
+          if (mw == -INFINITY) continue;
+          const float sc = exp2f(mw - mm);
+          ll += cr[D + 1] * sc;
+  #pragma unroll
+          for (int j = 0; j < CPT; ++j) acc[j] += cr[cl + 16 * j] * sc;
+        }
+        uint16_t* orow = a.o + (int64_t)b * a.ld_o + (int64_t)(g * a.group + row) * D + cl;
+        // the new key's state (score s_new, weight 1, value vnew) joins the
+        // pair's final combination
+        auto add_new_key = [&](float& m_, float& l_, float (&o_)[CPT]) {
+          const float mn = fmaxf(m_, s_new);
+          const float so = m_ == -INFINITY ? 0.f : exp2f(m_ - mn);
+          const float sn = exp2f(s_new - mn);
+          l_ = l_ * so + sn;
+  #pragma unroll
+          for (int j = 0; j < CPT; ++j) o_[j] = o_[j] * so + vnew[cl + 16 * j] * sn;
+          m_ = mn;
+        };
+        if (nseg == 1) {
+          if (a.qkv_pieces) add_new_key(mm, ll, acc);
+          if (row < a.group) store_out_row<CPT>(orow, acc, 1.f / ll);
+        } else {
+          const int first_c = owner(bg * TB);
+          const int my_slot = (pair_of(beg) == bg) ? 0 : 1;
+          float* rec = a.partials + (int64_t)(c * 2 + my_slot) * (16 * (D + 2));
+  #pragma unroll
+          for (int j = 0; j < CPT; ++j) rec[row * (D + 2) + cl + 16 * j] = acc[j];
+          if ((ctid & 15) == 0) { rec[row * (D + 2) + D] = mm; rec[row * (D + 2) + D + 1] = ll; }
+          // publish the record and take the pair's ticket: one thread fences
+          // for the CTA around the increment (the barriers carry the ordering)
+          bar_sync(1, kDecWarps * 32);
+          if (ctid == 0) {
+            fence_acq_rel_gpu();
+            const int old = atomicAdd(&a.tickets[bg], 1);
+            fence_acq_rel_gpu();
+            *last_flag = (old == nseg - 1) ? 1 : 0;
+          }
+          bar_sync(1, kDecWarps * 32);
+          if (*last_flag) {
+            float M2 = -INFINITY;
+            for (int sgi = 0; sgi < nseg; ++sgi) {
+              const int cc = first_c + sgi;
+              const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
+              const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
+              M2 = fmaxf(M2, __ldcg(&src[row * (D + 2) + D]));
+            }
+            float L2 = 0.f, acc2[CPT];
+  #pragma unroll
+            for (int j = 0; j < CPT; ++j) acc2[j] = 0.f;
+            for (int sgi = 0; sgi < nseg; ++sgi) {
+              const int cc = first_c + sgi;
+              const int slot = (pair_of(start_of(cc)) == bg) ? 0 : 1;
+              const float* src = a.partials + (int64_t)(cc * 2 + slot) * (16 * (D + 2));
+              const float ms = __ldcg(&src[row * (D + 2) + D]);
+              if (ms == -INFINITY) continue;
+              const float sc = exp2f(ms - M2);
+              L2 += __ldcg(&src[row * (D + 2) + D + 1]) * sc;
+  #pragma unroll
+              for (int j = 0; j < CPT; ++j) acc2[j] += __ldcg(&src[row * (D + 2) + cl + 16 * j]) * sc;
+            }
+            if (a.qkv_pieces) add_new_key(M2, L2, acc2);
+            if (row < a.group) store_out_row<CPT>(orow, acc2, 1.f / L2);
+            if (ctid == 0) a.tickets[bg] = 0;
+          }
         }
       }
       bar_sync(1, kDecWarps * 32);  // smem (q, comb, flag) reused by the next segment
