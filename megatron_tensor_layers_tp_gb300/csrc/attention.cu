@@ -372,6 +372,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) attn_decode_kernel(const __gri
         ++n;
         if (++u < end) advance();
       }
+      // The next kL2AheadUnits of this CTA's cache tiles go to L2 now, while
+      // the stages above wait for the prologue (at most 12 x 32 KB per CTA,
+      // well inside L2 over all SMs): a 64-key K or V tile is 16 KB
+      // contiguous in the cache ([copy][sequence][head][position][d]).  A
+      // prefetch only warms L2, the point of coherence, so rows this step
+      // still writes are read correctly later all the same.
+      {
+        constexpr int kL2AheadUnits = 12;
+        int pt = tile, pg = g, pb = b;
+        for (int64_t v = u; v < end && v < u + kL2AheadUnits; ++v) {
+          const int slice = ((pg / a.kv_r) * a.n_seqs + pb) * a.kv_r + (pg % a.kv_r);
+          const int p0 = pt * kKeyTile;
+          const int rows = min(kKeyTile, a.l_max - p0);
+          if (rows > 0) {
+            const int64_t off = ((int64_t)slice * a.l_max + p0) * D;
+            l2_prefetch_bulk(a.k_cache + off, static_cast<uint32_t>(rows) * D * 2);
+            l2_prefetch_bulk(a.v_cache + off, static_cast<uint32_t>(rows) * D * 2);
+          }
+          if (++pt == TB) {
+            pt = 0;
+            if (++pg == a.n_kv) { pg = 0; ++pb; }
+          }
+        }
+      }
       pdl_wait();
       for (; u < end; ++u) {
         const uint32_t s = n % S, ph = (n / S) & 1;

@@ -86,6 +86,14 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 }
 
 // ---------------------------------------------------------------- TMA
+// Bring `bytes` (a multiple of 16) of global memory at `p` (16-byte aligned)
+// into L2; nothing is written to shared memory and no barrier is involved.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -1116,6 +1116,8 @@ static tp_status prep_attention(const tp_model* m, const tp_batch_t* b, uint16_t
   a.ld_q = nhd;
   a.o = o;
   a.ld_o = nhd;
+  a.k_cache = kc;  // also the decode kernel's L2 prefetch of cache tiles
+  a.v_cache = vc;
   a.positions = b->positions;
   a.seq_start = b->seq_start;
   a.n_seqs = b->n_seqs;
