@@ -644,16 +644,22 @@ __global__ void __launch_bounds__(kThreadsOf<SWAP>, 1) gemm_kernel(const __grid_
       const uint64_t polA = make_policy(a.a_policy), polB = make_policy(a.b_policy);
       // decode orientation: A holds the weights; prefill orientation: B does.
       // (ks, kk): rank slice and 64-wide step inside it, kept as counters.
+      // The weights' tensor map is 4-D over the K-blocked shards (coordinates:
+      // 0, row, K block, rank); the activations' is 3-D (K, rows, slice).
       auto issue = [&](int g, int ia, int ib, int ks, int kk, uint32_t s, bool weights) {
         if (weights == SWAP) {
           const int sa = slice_of(a.a_slice_mode, g, ks);
-          if (a.a_slice_mid)
+          if constexpr (SWAP)
+            tma_load_4d(sA + s * kATileBytes, &a.tmA, &full[s], 0, ia * 128, kk, sa, polA);
+          else if (a.a_slice_mid)
             tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, sa, ia * 128, polA);
           else
             tma_load_3d(sA + s * kATileBytes, &a.tmA, &full[s], kk * 64, ia * 128, sa, polA);
         } else {
           const int sb = slice_of(a.b_slice_mode, g, ks);
-          if (a.b_slice_mid)
+          if constexpr (!SWAP)
+            tma_load_4d(sB + s * b_tile_bytes, &a.tmB, &full[s], 0, ib * BN, kk, sb, polB);
+          else if (a.b_slice_mid)
             tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, sb, ib * BN, polB);
           else
             tma_load_3d(sB + s * b_tile_bytes, &a.tmB, &full[s], kk * 64, ib * BN, sb, polB);

@@ -92,13 +92,10 @@ __global__ void __launch_bounds__(kPairThreads<EPI>, 1)
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the even CTA's full[0]
       auto load = [&](int g, int ia, int ib, int ks, int kk, uint32_t s, bool weights) {
         const uint32_t bar = full0 + s * 8;
-        if (weights) {
+        if (weights) {  // 4-D map over the K-blocked shards: (0, row, K block, rank)
           const int sb = slice_of(a.b_slice_mode, g, ks);
           const int r0 = ib * BN + static_cast<int>(rank) * HB;
-          if (a.b_slice_mid)
-            tma_load_3d_pair(sB + s * b_half_bytes, &a.tmB, bar, kk * 64, sb, r0, polB);
-          else
-            tma_load_3d_pair(sB + s * b_half_bytes, &a.tmB, bar, kk * 64, r0, sb, polB);
+          tma_load_4d_pair(sB + s * b_half_bytes, &a.tmB, bar, 0, r0, kk, sb, polB);
         } else {
           const int sa = slice_of(a.a_slice_mode, g, ks);
           const int r0 = ia * 256 + static_cast<int>(rank) * 128;

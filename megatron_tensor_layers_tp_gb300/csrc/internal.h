@@ -278,6 +278,8 @@ cudaError_t launch_fold_cols(uint16_t* dst, const uint16_t* src, const uint16_t*
 // else the other way round.  Waits for the preceding kernel first.
 cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, bool to_host,
                              cudaStream_t st);
+cudaError_t launch_reblock_k64(uint16_t* dst, const uint16_t* src, int ranks, int rows, int cols,
+                               cudaStream_t st);
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st);
 cudaError_t launch_stage_send(const uint16_t* src, uint16_t* dst, int M, int H, int t,

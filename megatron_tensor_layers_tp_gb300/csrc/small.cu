@@ -383,6 +383,34 @@ cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, bool to_h
                   static_cast<uint4*>(dst), n16);
 }
 
+// ---------------------------------------------------------------------------
+// Weight shards in K blocks: src [ranks][rows][cols] (row-major, cols % 64 ==
+// 0) -> dst [ranks][cols / 64][rows][64], so that the 128-byte row pieces of
+// one 64-wide K step are contiguous (a 128-row TMA box is then one 16 KB
+// run of memory instead of 128 pieces 2*cols bytes apart).  Block (row,
+// rank) moves its row; 8 threads per 128-byte piece.  Used once at load time.
+// ---------------------------------------------------------------------------
+__global__ void reblock_k64_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
+                                   int rows, int cols) {
+  const int row = blockIdx.x, rank = blockIdx.y;
+  const int64_t slice = (int64_t)rows * cols;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + rank * slice + (int64_t)row * cols);
+  uint16_t* d = dst + rank * slice + (int64_t)row * 64;
+  for (int v = threadIdx.x; v < cols / 8; v += blockDim.x) {
+    const int kb = v >> 3, part = v & 7;  // 64-wide block, 16-byte part of its 128 bytes
+    reinterpret_cast<uint4*>(d + (int64_t)kb * rows * 64)[part] = s4[v];
+  }
+}
+
+cudaError_t launch_reblock_k64(uint16_t* dst, const uint16_t* src, int ranks, int rows, int cols,
+                               cudaStream_t st) {
+  if (ranks == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  if (cols % 64 || (reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) % 16)
+    return cudaErrorInvalidValue;
+  reblock_k64_kernel<<<dim3(rows, ranks), 128, 0, st>>>(dst, src, rows, cols);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_rows(uint16_t* dst, int64_t dst_ld, const uint16_t* src, int64_t src_ld,
                              const int32_t* row_map, int n_rows, int n_cols, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;

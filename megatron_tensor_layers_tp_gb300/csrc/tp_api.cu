@@ -115,6 +115,25 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of a weight shard stored in K blocks, [ranks][cols / 64][rows][64]
+// bf16: dims (64, rows, cols / 64, ranks), box (64, box_rows, 1, 1), 128-byte
+// swizzle.  A box at (0, row, K block, rank) is box_rows x 128 contiguous
+// bytes, the same tile (and shared-memory image) the row-major layout's
+// (K step x 64, row, rank) box gives.
+bool make_tmap_kblocked(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint64_t ranks, uint32_t box_rows) {
+  auto enc = get_encoder();
+  if (!enc || cols % 64) return false;
+  cuuint64_t dims[4] = {64, rows, cols / 64, ranks};
+  cuuint64_t strides[3] = {128, rows * 128, rows * cols * 2};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 tp_status cuda_status(cudaError_t e) {
@@ -575,19 +594,35 @@ bool valid_layer(const tp_model* m, int layer) {
   return m && layer >= 0 && layer < (int)m->layers.size();
 }
 
-// Builds one sharded weight: t ranks of [rows][cols]; rank r's rows come from
-// the calls the caller makes through `fill` (copy_rows launches).
+// One sharded weight of `ranks` x [rows][cols].  The loader fills it row-major
+// (copy_rows launches); reblock_linear then moves it into K blocks and encodes
+// its tensor maps.
 tp_status alloc_linear(tp_model* m, ShardedLinear* L, int rows, int cols, int ranks) {
   L->rows = rows;
   L->cols = cols;
   L->ranks = ranks;
-  tp_status s = dev_alloc(m, &L->data, (size_t)ranks * rows * cols * 2);
+  return dev_alloc(m, &L->data, (size_t)ranks * rows * cols * 2);
+}
+
+// Row-major shard -> [ranks][cols / 64][rows][64] (a new buffer; the old one
+// is freed) and the tensor maps of both GEMM orientations over it.  Measured
+// in isolation (8-stage TMA ring, 152 CTAs, a [28672][4096] bf16 matrix):
+// 37.7 us row-major, 36.4 us in K blocks.
+tp_status reblock_linear(tp_model* m, ShardedLinear* L, cudaStream_t st) {
+  uint16_t* kb = nullptr;
+  tp_status s = dev_alloc(m, &kb, (size_t)L->ranks * L->rows * L->cols * 2);
   if (s != TP_OK) return s;
-  const uint64_t rs = (uint64_t)cols * 2, ss = (uint64_t)rows * cols * 2;
-  if (!make_tmap(&L->tm_a, L->data, cols, rows, ranks, rs, ss, 128)) return TP_ERR_CUDA;
+  if (launch_reblock_k64(kb, L->data, L->ranks, L->rows, L->cols, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    dev_free(m, kb);
+    return TP_ERR_CUDA;
+  }
+  dev_free(m, L->data);
+  L->data = kb;
+  if (!make_tmap_kblocked(&L->tm_a, L->data, L->rows, L->cols, L->ranks, 128)) return TP_ERR_CUDA;
   for (int i = 0; i < kNumPrefillBN; ++i) {
-    if (!make_tmap(&L->tm_b[i], L->data, cols, rows, ranks, rs, ss, kPrefillBNs[i])) return TP_ERR_CUDA;
-    if (!make_tmap(&L->tm_h[i], L->data, cols, rows, ranks, rs, ss, kPrefillBNs[i] / 2))
+    if (!make_tmap_kblocked(&L->tm_b[i], L->data, L->rows, L->cols, L->ranks, kPrefillBNs[i]) ||
+        !make_tmap_kblocked(&L->tm_h[i], L->data, L->rows, L->cols, L->ranks, kPrefillBNs[i] / 2))
       return TP_ERR_CUDA;
   }
   return TP_OK;
@@ -927,6 +962,7 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
     // the norms' weights folded into the column-parallel GEMMs that read them;
     // a norm weight of exactly 1 leaves the shard unchanged, and then the one
     // buffer serves the decoder layer and tp_column_linear alike
+    bool shared_fold[2] = {false, false};  // the folded shard is the plain one
     for (int which = 0; which < 2; ++which) {
       ShardedLinear& plain = which == 0 ? Ls.qkv : Ls.gate_up;
       ShardedLinear& folded = which == 0 ? Ls.qkv_folded : Ls.gate_up_folded;
@@ -938,7 +974,7 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
       bool unit = true;
       for (uint16_t v : hw) unit = unit && v == 0x3F80;  // bf16 1.0
       if (unit) {
-        folded = plain;
+        shared_fold[which] = true;
         continue;
       }
       if ((s = alloc_linear(m, &folded, plain.rows, H, plain.ranks)) != TP_OK) return fail(s);
@@ -953,6 +989,11 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
         plain.data = nullptr;
       }
     }
+    // every shard of the layer into K blocks
+    for (ShardedLinear* Lw : {&Ls.qkv, &Ls.gate_up, &Ls.o, &Ls.down, &Ls.qkv_folded, &Ls.gate_up_folded})
+      if (Lw->data && (s = reblock_linear(m, Lw, st)) != TP_OK) return fail(s);
+    if (shared_fold[0]) Ls.qkv_folded = Ls.qkv;
+    if (shared_fold[1]) Ls.gate_up_folded = Ls.gate_up;
   }
   {
     const std::vector<uint16_t> one(H, 0x3F80);  // bf16 1.0
@@ -975,6 +1016,7 @@ tp_status tp_load_shards(const tp_config_t* cfg_in, const tp_weights_t* w, void*
       if ((s = alloc_linear(m, &m->lm, cfg.vocab_per_rank, H, t)) != TP_OK) return fail(s);
       if (launch_copy_rows(m->lm.data, H, w->lm_head, H, dmv, cfg.vocab_padded, H, st) != cudaSuccess)
         return fail(TP_ERR_CUDA);
+      if ((s = reblock_linear(m, &m->lm, st)) != TP_OK) return fail(s);
     }
   }
   if (w->final_norm) {
